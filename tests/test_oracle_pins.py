@@ -1,0 +1,332 @@
+"""Pins for the CPU oracle: each test checks it against something other than
+itself (a library routine, exact rational arithmetic, a published table, an
+invariant of the mathematics), chosen so that a plausible slip anywhere in the
+oracle (a wrong table entry, nibble order, scale index, sign, dropped term,
+transposed operand, double rounding) fails at least one of them.
+
+The operation is FlashInfer's grouped_gemm_nt_masked as the page "The
+CuteDSL Gamble: Chasing Kernel Efficiency on Blackwell GPUs" describes it
+(sections "The Message" and "Output Knowledge Created").
+"""
+import json
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import oracle
+from nvfp4_block_scaled_masked_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+# e2m1 magnitudes as printed in the OCP Microscaling Formats (MX) v1.0
+# specification's FP4 (E2M1) element format (see tests/golden/ocp_formats.json)
+with open(os.path.join(GOLDEN, "ocp_formats.json")) as f:
+    OCP = json.load(f)
+
+
+# ---------------------------------------------------------------- P1 tables
+
+def test_e2m1_all_codes_match_ocp_table():
+    mags = [Fraction(x) for x in OCP["e2m1_magnitudes_by_low3bits"]]
+    for code in range(16):
+        want = mags[code & 7] * (-1 if code & 8 else 1)
+        got = oracle.e2m1_value(code)
+        assert got == float(want), (code, got, want)
+        assert np.copysign(1.0, got) == (-1.0 if code & 8 else 1.0)
+    np.testing.assert_array_equal(oracle.E2M1_TABLE, [oracle.e2m1_value(c) for c in range(16)])
+
+
+def test_e4m3_all_bytes_match_torch_float8_e4m3fn():
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    got = np.array([oracle.e4m3_value(b) for b in range(256)])
+    nan = np.isnan(lib)
+    assert np.array_equal(np.isnan(got), nan)
+    assert list(np.flatnonzero(nan)) == [0x7F, 0xFF]
+    np.testing.assert_array_equal(got[~nan], lib[~nan])
+    np.testing.assert_array_equal(oracle.E4M3_TABLE[~nan], lib[~nan])
+
+
+def test_e4m3_spot_values_from_ocp():
+    for hexbyte, val in OCP["e4m3_spot_values"].items():
+        assert oracle.e4m3_value(int(hexbyte, 16)) == float(Fraction(val)), hexbyte
+
+
+def test_bf16_rne_matches_torch_on_float32_values():
+    rng = np.random.default_rng(7)
+    x = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32) * np.float32(1000),
+        (rng.standard_normal(2000) * 1e-30).astype(np.float32),
+        np.array([1.0, -1.0, 3.0, 65504.0, 1e38, -1e38, 2.0 ** -126], dtype=np.float32),
+    ])
+    want = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    got = np.array([oracle.bf16_rne(float(v)) for v in x], dtype=np.uint16)
+    np.testing.assert_array_equal(got, want)
+    # the NumPy restatement agrees on the normal range
+    normal = np.abs(x) >= 2.0 ** -126
+    np.testing.assert_array_equal(oracle.bf16_bits_numpy(x[normal].astype(np.float64)), want[normal])
+
+
+def test_bf16_rne_rounds_once_from_fp64():
+    # 1 + 2^-8 is exactly halfway between bf16 1.0 and 1 + 2^-7: ties to even
+    assert oracle.bf16_rne(1.0 + 2.0 ** -8) == 0x3F80
+    # slightly above the tie must round up; going through fp32 first would
+    # lose the 2^-30 and round down to even
+    assert oracle.bf16_rne(1.0 + 2.0 ** -8 + 2.0 ** -30) == 0x3F81
+    assert oracle.bf16_rne(-(1.0 + 2.0 ** -8 + 2.0 ** -30)) == 0xBF81
+    # odd neighbour: 1 + 3*2^-8 ties to the even 1 + 2^-6
+    assert oracle.bf16_rne(1.0 + 3 * 2.0 ** -8) == 0x3F82
+    # carry into the next binade
+    assert oracle.bf16_rne(2.0 - 2.0 ** -9) == 0x4000
+    assert oracle.bf16_rne(0.0) == 0 and oracle.bf16_rne(-0.0) == 0x8000
+
+
+# ------------------------------------------------ exact rational brute force
+
+def _bf16_exact(fr: Fraction) -> int:
+    """bf16 bits of the exact rational, one rounding, ties to even."""
+    if fr == 0:
+        return 0
+    sign = 0x8000 if fr < 0 else 0
+    a = abs(fr)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    q = Fraction(2) ** (max(e, -126) - 7)
+    r = round(a / q) * q          # Fraction round(): half to even
+    bits = np.array([float(r)], dtype=np.float32).view(np.uint32)[0] >> 16
+    return sign | int(bits)
+
+
+def _elem_exact(codes_row, sf_row, k):
+    byte = int(codes_row[k // 2])
+    code = (byte >> 4) if k % 2 else (byte & 15)
+    mag = Fraction(OCP["e2m1_magnitudes_by_low3bits"][code & 7])
+    s = int(sf_row[k // 16])
+    e, m = (s >> 3) & 15, s & 7
+    sc = Fraction(m, 512) if e == 0 else Fraction(8 + m, 8) * Fraction(2) ** (e - 7)
+    return (-mag if code & 8 else mag) * sc
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_oracle_equals_exact_rational_arithmetic(seed):
+    """Tiny shapes, any finite positive e4m3 scale (subnormals included), any
+    codes: the oracle's fp64 value must equal alpha times the exact rational
+    sum correctly rounded, and C its bf16 rounding."""
+    rng = np.random.default_rng(seed)
+    G, M, N, K = 2, 3, 4, 48
+    A = rng.integers(0, 256, (G, M, K // 2), dtype=np.uint8)
+    B = rng.integers(0, 256, (G, N, K // 2), dtype=np.uint8)
+    A_sf = rng.integers(0, 0x7F, (G, M, K // 16), dtype=np.uint8)   # 0x00..0x7E
+    B_sf = rng.integers(0, 0x7F, (G, N, K // 16), dtype=np.uint8)
+    alpha = rng.uniform(0.5, 2.0, G).astype(np.float32)
+    mm = np.array([3, 2], dtype=np.int32)
+    C0 = np.full((G, M, N), 0x7FC0, dtype=np.uint16)
+    C, ref = oracle.gemm(A, A_sf, B, B_sf, alpha, mm, C0, G, M, N, K)
+    for g in range(G):
+        for m in range(M):
+            for n in range(N):
+                if m >= mm[g]:
+                    assert C[g, m, n] == 0x7FC0 and np.isnan(ref[g, m, n])
+                    continue
+                s = sum(_elem_exact(A[g, m], A_sf[g, m], k) * _elem_exact(B[g, n], B_sf[g, n], k)
+                        for k in range(K))
+                exact = Fraction(float(alpha[g])) * s
+                assert ref[g, m, n] == float(exact)
+                assert C[g, m, n] == _bf16_exact(exact), (g, m, n)
+
+
+def test_single_nonzero_brute_force():
+    """Every code pair x every scale pair of the workload set x every position
+    k of a K=32 row, one non-zero per row: C must be the exact product (<= 4
+    significant bits, so bf16-exact), which pins nibble order and the k/16
+    scale index."""
+    codes = np.arange(16)
+    sc = W.SCALE_BYTES
+    ca, cb, ia, ib, pos = np.meshgrid(codes, codes, np.arange(len(sc)), np.arange(len(sc)),
+                                      np.arange(32), indexing="ij")
+    ca, cb, ia, ib, pos = (x.ravel() for x in (ca, cb, ia, ib, pos))
+    G = ca.size
+    K = 32
+    A = np.zeros((G, 1, K // 2), dtype=np.uint8)
+    B = np.zeros((G, 1, K // 2), dtype=np.uint8)
+    rows = np.arange(G)
+    shift = (pos % 2) * 4
+    A[rows, 0, pos // 2] = (ca << shift).astype(np.uint8)
+    B[rows, 0, pos // 2] = (cb << shift).astype(np.uint8)
+    # the block holding pos gets the drawn scale; the other block a decoy
+    A_sf = np.full((G, 1, 2), 0x48, dtype=np.uint8)
+    B_sf = np.full((G, 1, 2), 0x18, dtype=np.uint8)
+    A_sf[rows, 0, pos // 16] = sc[ia]
+    B_sf[rows, 0, pos // 16] = sc[ib]
+    alpha = np.ones(G, dtype=np.float32)
+    mm = np.ones(G, dtype=np.int32)
+    C, ref = oracle.gemm(A, A_sf, B, B_sf, alpha, mm, np.zeros((G, 1, 1), np.uint16), G, 1, 1, K)
+    e2m1 = np.array([float(Fraction(OCP["e2m1_magnitudes_by_low3bits"][c & 7])) * (-1 if c & 8 else 1)
+                     for c in range(16)])
+    e4m3 = torch.from_numpy(sc.copy()).view(torch.float8_e4m3fn).double().numpy()
+    want = e2m1[ca] * e2m1[cb] * e4m3[ia] * e4m3[ib]
+    np.testing.assert_array_equal(ref[:, 0, 0], want)
+    want_bits = torch.from_numpy(want).float().to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    got = C[:, 0, 0]
+    # +0 and -0 are both correct for an exact zero
+    zero = want == 0
+    np.testing.assert_array_equal(got[~zero], want_bits[~zero])
+    assert np.all((got[zero] == 0) | (got[zero] == 0x8000))
+
+
+def test_integer_special_case_is_int64_matmul():
+    """All scales 1.0 (0x38), alpha 1, codes for 0, 1, -1, 2: C must be the
+    integer matrix product (numpy int64 matmul), rounded to bf16."""
+    rng = np.random.default_rng(11)
+    G, M, N, K = 3, 5, 7, 64
+    vals = np.array([0, 1, -1, 2])
+    codes = np.array([0x0, 0x2, 0xA, 0x4], dtype=np.uint8)
+    ia = rng.integers(0, 4, (G, M, K))
+    ib = rng.integers(0, 4, (G, N, K))
+    pack = lambda i: (codes[i[..., 0::2]] | (codes[i[..., 1::2]] << 4)).astype(np.uint8)
+    A, B = pack(ia), pack(ib)
+    A_sf = np.full((G, M, K // 16), 0x38, np.uint8)
+    B_sf = np.full((G, N, K // 16), 0x38, np.uint8)
+    mm = np.array([5, 0, 3], dtype=np.int32)
+    C, ref = oracle.gemm(A, A_sf, B, B_sf, np.ones(G, np.float32), mm,
+                         np.full((G, M, N), 0x7FC0, np.uint16), G, M, N, K)
+    for g in range(G):
+        want = vals[ia[g]].astype(np.int64) @ vals[ib[g]].astype(np.int64).T
+        np.testing.assert_array_equal(ref[g, :mm[g]], want[:mm[g]])
+        bits = torch.from_numpy(want[:mm[g]]).float().to(torch.bfloat16).view(torch.int16).numpy()
+        np.testing.assert_array_equal(C[g, :mm[g]], bits.astype(np.uint16))
+        assert np.all(C[g, mm[g]:] == 0x7FC0)
+
+
+def test_short_k_float32_sum_is_exact():
+    """With the workload's power-of-two scales and K <= 28 every partial sum
+    is exact in fp32 too: the oracle's fp64 result equals a float32 BLAS
+    product of the decoded operands bit for bit (the exactness argument)."""
+    cfg = W.custom(2, 6, 8, 16, masked_m=[6, 4])
+    d = W.generate(cfg, seed=5)
+    C, ref = oracle.gemm(d["A"], d["A_sf"], d["B"], d["B_sf"], np.ones(2, np.float32),
+                         d["masked_m"], d["C_init"], 2, 6, 8, 16)
+    Ad = oracle.decode_numpy(d["A"], d["A_sf"], 16).astype(np.float32)
+    Bd = oracle.decode_numpy(d["B"], d["B_sf"], 16).astype(np.float32)
+    for g in range(2):
+        m = d["masked_m"][g]
+        f32 = (Ad[g, :m] @ Bd[g].T).astype(np.float64)
+        np.testing.assert_array_equal(ref[g, :m], f32)
+
+
+# ------------------------------------------------------- second implementation
+
+@pytest.mark.parametrize("key", ["c1"])
+def test_c_oracle_matches_numpy_restatement(key):
+    cfg = W.CONFIGS[key]
+    d = W.generate(cfg)
+    args = (d["A"], d["A_sf"], d["B"], d["B_sf"], d["alpha"], d["masked_m"], d["C_init"],
+            cfg.G, cfg.M_max, cfg.N, cfg.K)
+    C1, r1 = oracle.gemm(*args)
+    C2, r2 = oracle.gemm_numpy(*args)
+    np.testing.assert_array_equal(C1, C2)
+    np.testing.assert_array_equal(r1, r2)
+
+
+def test_sampled_matches_full():
+    cfg = W.CONFIGS["c1"]
+    d = W.generate(cfg)
+    C, ref = oracle.gemm(d["A"], d["A_sf"], d["B"], d["B_sf"], d["alpha"], d["masked_m"],
+                         d["C_init"], cfg.G, cfg.M_max, cfg.N, cfg.K)
+    rng = np.random.default_rng(0)
+    idx = []
+    for g in range(cfg.G):
+        for _ in range(50):
+            if d["masked_m"][g]:
+                idx.append((g, rng.integers(d["masked_m"][g]), rng.integers(cfg.N)))
+    idx = np.array(idx)
+    s = oracle.gemm_sampled(d["A"], d["A_sf"], d["B"], d["B_sf"], d["alpha"], idx,
+                            cfg.G, cfg.M_max, cfg.N, cfg.K)
+    np.testing.assert_array_equal(s, ref[idx[:, 0], idx[:, 1], idx[:, 2]])
+
+
+# ------------------------------------------------------------------ invariants
+
+def _run(d, cfg, alpha=None):
+    return oracle.gemm(d["A"], d["A_sf"], d["B"], d["B_sf"],
+                       d["alpha"] if alpha is None else alpha, d["masked_m"], d["C_init"],
+                       cfg.G, cfg.M_max, cfg.N, cfg.K)
+
+
+def _bf16_to_f64(bits):
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("j", [-2, 1])
+def test_alpha_power_of_two_linearity(j):
+    cfg = W.CONFIGS["c1"]
+    d = W.generate(cfg)
+    C, _ = _run(d, cfg)
+    Cj, _ = _run(d, cfg, alpha=(d["alpha"] * np.float32(2.0 ** j)).astype(np.float32))
+    for g in range(cfg.G):
+        m = d["masked_m"][g]
+        np.testing.assert_array_equal(_bf16_to_f64(Cj[g, :m]), _bf16_to_f64(C[g, :m]) * 2.0 ** j)
+
+
+def test_masked_rows_and_empty_groups_untouched_and_poison_ignored():
+    cfg = W.CONFIGS["c1"]
+    d = W.generate(cfg)
+    p = W.generate(cfg, poison=True)
+    C, _ = _run(d, cfg)
+    Cp, _ = _run(p, cfg)
+    for g in range(cfg.G):
+        m = d["masked_m"][g]
+        assert np.all(C[g, m:] == W.SENTINEL_BF16)
+        valid = C[g, :m]
+        assert not np.any(valid == W.SENTINEL_BF16)
+        assert np.all(np.isfinite(_bf16_to_f64(valid)))
+    np.testing.assert_array_equal(C, Cp)
+    assert d["masked_m"][0] == 0 and np.all(C[0] == W.SENTINEL_BF16)
+
+
+def test_permutation_symmetry():
+    cfg = W.custom(3, 8, 32, 64, masked_m=[8, 3, 5])
+    d = W.generate(cfg, seed=3)
+    C, _ = _run(d, cfg)
+    perm = np.array([2, 0, 1])
+    q = {k: (v[perm] if isinstance(v, np.ndarray) and v.shape[:1] == (3,) else v) for k, v in d.items()}
+    cfgp = W.custom(3, 8, 32, 64, masked_m=d["masked_m"][perm])
+    Cp, _ = _run(q, cfgp)
+    np.testing.assert_array_equal(Cp, C[perm])
+    # permuting the rows of B permutes the columns of C
+    cols = np.random.default_rng(0).permutation(32)
+    r = dict(d)
+    r["B"], r["B_sf"] = d["B"][:, cols], d["B_sf"][:, cols]
+    Cc, _ = _run(r, cfg)
+    np.testing.assert_array_equal(Cc, C[:, :, cols])
+
+
+def test_oracle_rejects_bad_arguments():
+    cfg = W.custom(1, 4, 8, 32, masked_m=[5])   # masked_m > M_max
+    with pytest.raises(AssertionError):
+        W.generate(cfg)
+    d = W.generate(W.custom(1, 4, 8, 32, masked_m=[4]))
+    with pytest.raises(ValueError):
+        oracle.gemm(d["A"], d["A_sf"], d["B"], d["B_sf"], d["alpha"], np.array([5], np.int32),
+                    d["C_init"], 1, 4, 8, 32)
+
+
+# --------------------------------------------------------------- golden fixture
+
+def test_golden_tiny_case_regression():
+    """A tiny case frozen by tests/golden/make_golden.py (which calls only the
+    oracle): inputs and expected output bits are stored as hex text."""
+    with open(os.path.join(GOLDEN, "tiny_case.json")) as f:
+        gd = json.load(f)
+    G, M, N, K = gd["G"], gd["M_max"], gd["N"], gd["K"]
+    h = lambda s, shape: np.frombuffer(bytes.fromhex(s), dtype=np.uint8).reshape(shape)
+    A, A_sf = h(gd["A"], (G, M, K // 2)), h(gd["A_sf"], (G, M, K // 16))
+    B, B_sf = h(gd["B"], (G, N, K // 2)), h(gd["B_sf"], (G, N, K // 16))
+    alpha = np.array(gd["alpha"], dtype=np.float32)
+    mm = np.array(gd["masked_m"], dtype=np.int32)
+    C, ref = oracle.gemm(A, A_sf, B, B_sf, alpha, mm, np.full((G, M, N), 0x7FC0, np.uint16),
+                         G, M, N, K)
+    np.testing.assert_array_equal(C.ravel(), np.array(gd["C_bits"], dtype=np.uint16))
