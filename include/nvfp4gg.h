@@ -1,0 +1,157 @@
+/*
+ * nvfp4gg — masked, block-scaled NVFP4 grouped GEMM-NT for GB300 (sm_103a).
+ *
+ * The operation is the one FlashInfer exposes as grouped_gemm_nt_masked, as
+ * described on the page "The CuteDSL Gamble: Chasing Kernel Efficiency on
+ * Blackwell GPUs" (sections "The Message" and "Output Knowledge Created"):
+ * a masked, batched GEMM whose operands each come as (data, block scale
+ * factors), with one valid-row count masked_m[g] per expert and an optional
+ * alpha applied at the output.  For every expert g < G, every row
+ * m < masked_m[g] and every n < N:
+ *
+ *     C[g][m][n] = bf16( alpha[g] * sum_{k<K} A[g][m][k] * B[g][n][k] )
+ *
+ * where each A/B element is an e2m1 (FP4) code times the e4m3 scale of its
+ * 16-element block along K (sf_vec_size = 16, i.e. NVFP4).  "NT" means both
+ * operands are K-major: A is [G][M_max][K], B is [G][N][K].  Rows of C at or
+ * past masked_m[g] are never written.
+ *
+ * Encodings (the pages name NVFP4 but do not define it; these are the OCP
+ * Microscaling readings):
+ *   e2m1: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa; two codes
+ *         per byte, element k of a row in byte k/2, even k in the low nibble.
+ *   e4m3: one byte per 16 K-elements, positive finite values (bit 7 clear,
+ *         not 0x7F).
+ *   C:    bf16, round to nearest even.
+ *
+ * Conventions for every call:
+ *   - All buffers are owned by the caller.  The library allocates no device
+ *     memory in any call.
+ *   - Device pointers must be 16-byte aligned (alpha and masked_m: 4-byte).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream) and never synchronise the host, except
+ *     nvfp4_gg_check_error.  masked_m is never read on the host.
+ *   - Every entry point checks its arguments on the host first and returns a
+ *     negative nvfp4gg_status without launching anything when they are bad.
+ *   - Calls on one stream are thread-compatible; the SM cap set by
+ *     nvfp4_gg_set_sm_count is process-wide.
+ */
+#ifndef NVFP4GG_H
+#define NVFP4GG_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4GG_OK = 0,
+    NVFP4GG_ERR_NULL = -1,      /* a required pointer is NULL                        */
+    NVFP4GG_ERR_SHAPE = -2,     /* G, M_max, N or K outside the supported set         */
+    NVFP4GG_ERR_ALIGN = -3,     /* a pointer is not aligned as required              */
+    NVFP4GG_ERR_ARCH = -4,      /* the current device is not compute capability 10.3 */
+    NVFP4GG_ERR_CUDA = -5,      /* a CUDA runtime/driver call failed                 */
+    NVFP4GG_ERR_TIMEOUT = -6,   /* a device-side wait ran past its limit (error word) */
+    NVFP4GG_ERR_MASK = -7       /* masked_m[g] outside [0, M_max] seen on the device  */
+} nvfp4gg_status;
+
+/* Shape limits of nvfp4_grouped_gemm_nt_masked. */
+#define NVFP4GG_MAX_GROUPS 1024   /* 1 <= G <= 1024                                  */
+#define NVFP4GG_K_ALIGN 256       /* K % 256 == 0 (a 16-byte row of A_sf per 256 K)   */
+#define NVFP4GG_N_ALIGN 16        /* N % 16 == 0                                      */
+
+/*
+ * Sizes of the prepared weight buffers that nvfp4_prepare_weights writes.
+ *   *b_bytes  = G * N * K / 2                        (codes, same layout as B)
+ *   *sf_bytes = G * ceil(N/128) * (K/64) * 512       (scales in MMA atom order)
+ * Returns NVFP4GG_OK or NVFP4GG_ERR_NULL / NVFP4GG_ERR_SHAPE.
+ */
+int nvfp4_prepared_weight_bytes(int G, int N, int K, size_t* b_bytes, size_t* sf_bytes);
+
+/*
+ * One-time weight re-layout (run once per weight set, outside the timed GEMM).
+ *   B         device u8 [G][N][K/2]   e2m1 codes, K-major
+ *   B_sf      device u8 [G][N][K/16]  e4m3 scales, row-major
+ *   B_prep    device, b_bytes:  receives the codes (a copy of B; B_prep == B
+ *             is allowed and then nothing is copied)
+ *   B_sf_prep device, sf_bytes: receives the scales regrouped into 512-byte
+ *             atoms, one per (expert, 128-row block of N, 64-element block of
+ *             K): byte (i*16 + j*4 + b) of an atom holds the scale of row
+ *             128*nb + 32*j + i and K block 4*kc + b (zero past row N).
+ * Asynchronous on `stream`.  B_sf_prep must not alias B_sf.
+ */
+int nvfp4_prepare_weights(const void* B, const void* B_sf, int G, int N, int K,
+                          void* B_prep, void* B_sf_prep, void* stream);
+
+/*
+ * The grouped GEMM.
+ *   A        device u8 [G][M_max][K/2]   e2m1 activations (rows >= masked_m[g]
+ *            may hold anything, including NaN scales; they are ignored)
+ *   A_sf     device u8 [G][M_max][K/16]  e4m3 activation scales, row-major
+ *   B        device, prepared codes  (nvfp4_prepare_weights)
+ *   B_sf     device, prepared scales (nvfp4_prepare_weights)
+ *   alpha    device f32 [G]
+ *   masked_m device i32 [G], 0 <= masked_m[g] <= M_max (values outside are
+ *            clamped and flagged NVFP4GG_ERR_MASK in the error word)
+ *   C        device bf16 [G][M_max][N], row-major; rows m >= masked_m[g] keep
+ *            their previous contents bit for bit
+ * Limits: 1 <= G <= NVFP4GG_MAX_GROUPS, M_max >= 1, N % 16 == 0,
+ * K % 256 == 0.  Asynchronous on `stream`; device-side failures (a wait past
+ * its time limit, a bad masked_m) are recorded in the error word read by
+ * nvfp4_gg_check_error.
+ */
+int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
+                                 const void* B_sf, const float* alpha, const int* masked_m,
+                                 void* C, int G, int M_max, int N, int K, void* stream);
+
+/*
+ * End-to-end variant for callers whose activations live in host memory.
+ *   h_A, h_A_sf, h_alpha, h_masked_m: HOST buffers laid out as above (pinned
+ *       memory gives asynchronous copies)
+ *   B, B_sf: DEVICE prepared weights
+ *   h_C: HOST bf16 [G][M_max][N]; only rows m < h_masked_m[g] are written
+ *   d_staging: DEVICE scratch of at least nvfp4_host_staging_bytes(...) bytes,
+ *       16-byte aligned, owned by the caller
+ * Copies the inputs host->device, runs the GEMM, copies the valid rows of C
+ * device->host (one copy per non-empty expert), all on `stream`.  Returns
+ * when the work is queued; synchronise `stream` before reading h_C.
+ */
+size_t nvfp4_host_staging_bytes(int G, int M_max, int N, int K);
+int nvfp4_grouped_gemm_nt_masked_host(const void* h_A, const void* h_A_sf,
+                                      const float* h_alpha, const int* h_masked_m,
+                                      const void* B, const void* B_sf, void* h_C,
+                                      int G, int M_max, int N, int K,
+                                      void* d_staging, size_t staging_bytes, void* stream);
+
+/*
+ * Caps the number of SMs (persistent CTAs) a GEMM launch uses; 0 = all SMs.
+ * This is the sm_count argument of grouped_gemm_nt_masked on the same page
+ * ("The Message").  Process-wide.  Returns NVFP4GG_ERR_SHAPE if negative.
+ */
+int nvfp4_gg_set_sm_count(int sm_count);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's error
+ * word.  Returns NVFP4GG_OK, NVFP4GG_ERR_TIMEOUT, NVFP4GG_ERR_MASK, or
+ * NVFP4GG_ERR_CUDA if a CUDA call failed.
+ */
+int nvfp4_gg_check_error(void* stream);
+
+/*
+ * Launches one CTA that waits on a barrier nothing ever completes, with the
+ * same bounded-wait code the GEMM uses and the given limit in nanoseconds
+ * (1e3 .. 1e10).  The wait gives up, records NVFP4GG_ERR_TIMEOUT in the
+ * error word and the kernel returns; nvfp4_gg_check_error then reports it.
+ * Used to test the watchdog without faulting or hanging the GPU.
+ */
+int nvfp4_gg_selftest_watchdog(long long timeout_ns, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* nvfp4_gg_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4GG_H */

@@ -1,0 +1,158 @@
+"""Python binding of libnvfp4gg (include/nvfp4gg.h): argument marshalling only.
+
+Every function takes device buffers as torch tensors (their data_ptr is
+passed) or as raw integer addresses, and a CUDA stream (a torch.cuda.Stream,
+a raw cudaStream_t integer, or None for torch's current stream).  All work
+runs in the library's CUDA kernels; if the library is not built this module
+raises instead of computing anything another way.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+_lib = None
+
+OK = 0
+ERR_NULL = -1
+ERR_SHAPE = -2
+ERR_ALIGN = -3
+ERR_ARCH = -4
+ERR_CUDA = -5
+ERR_TIMEOUT = -6
+ERR_MASK = -7
+
+# every symbol the header declares
+EXPORTS = (
+    "nvfp4_prepared_weight_bytes",
+    "nvfp4_prepare_weights",
+    "nvfp4_grouped_gemm_nt_masked",
+    "nvfp4_host_staging_bytes",
+    "nvfp4_grouped_gemm_nt_masked_host",
+    "nvfp4_gg_set_sm_count",
+    "nvfp4_gg_check_error",
+    "nvfp4_gg_selftest_watchdog",
+    "nvfp4_gg_status_string",
+)
+
+
+class NVFP4GGError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load():
+    """Open libnvfp4gg.so (built in-tree by __graft_entry__.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    vp, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.nvfp4_prepared_weight_bytes.argtypes = [i, i, i, ctypes.POINTER(sz), ctypes.POINTER(sz)]
+    lib.nvfp4_prepared_weight_bytes.restype = i
+    lib.nvfp4_prepare_weights.argtypes = [vp, vp, i, i, i, vp, vp, vp]
+    lib.nvfp4_prepare_weights.restype = i
+    lib.nvfp4_grouped_gemm_nt_masked.argtypes = [vp] * 7 + [i] * 4 + [vp]
+    lib.nvfp4_grouped_gemm_nt_masked.restype = i
+    lib.nvfp4_host_staging_bytes.argtypes = [i] * 4
+    lib.nvfp4_host_staging_bytes.restype = sz
+    lib.nvfp4_grouped_gemm_nt_masked_host.argtypes = [vp] * 7 + [i] * 4 + [vp, sz, vp]
+    lib.nvfp4_grouped_gemm_nt_masked_host.restype = i
+    lib.nvfp4_gg_set_sm_count.argtypes = [i]
+    lib.nvfp4_gg_set_sm_count.restype = i
+    lib.nvfp4_gg_check_error.argtypes = [vp]
+    lib.nvfp4_gg_check_error.restype = i
+    lib.nvfp4_gg_selftest_watchdog.argtypes = [ctypes.c_longlong, vp]
+    lib.nvfp4_gg_selftest_watchdog.restype = i
+    lib.nvfp4_gg_status_string.argtypes = [i]
+    lib.nvfp4_gg_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):          # numpy array (host buffers)
+        return x.ctypes.data
+    raise TypeError(f"cannot take the address of {type(x)}")
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise NVFP4GGError(rc, what)
+
+
+def status_string(status: int) -> str:
+    return load().nvfp4_gg_status_string(int(status)).decode()
+
+
+def nvfp4_prepared_weight_bytes(G: int, N: int, K: int):
+    b, s = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(load().nvfp4_prepared_weight_bytes(G, N, K, ctypes.byref(b), ctypes.byref(s)),
+           "nvfp4_prepared_weight_bytes")
+    return b.value, s.value
+
+
+def nvfp4_prepare_weights(B, B_sf, G, N, K, B_prep, B_sf_prep, stream=None):
+    _check(load().nvfp4_prepare_weights(_ptr(B), _ptr(B_sf), G, N, K, _ptr(B_prep),
+                                        _ptr(B_sf_prep), _stream(stream)),
+           "nvfp4_prepare_weights")
+
+
+def nvfp4_grouped_gemm_nt_masked(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K,
+                                 stream=None):
+    _check(load().nvfp4_grouped_gemm_nt_masked(_ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf),
+                                               _ptr(alpha), _ptr(masked_m), _ptr(C),
+                                               G, M_max, N, K, _stream(stream)),
+           "nvfp4_grouped_gemm_nt_masked")
+
+
+def nvfp4_host_staging_bytes(G, M_max, N, K) -> int:
+    return int(load().nvfp4_host_staging_bytes(G, M_max, N, K))
+
+
+def nvfp4_grouped_gemm_nt_masked_host(h_A, h_A_sf, h_alpha, h_masked_m, B, B_sf, h_C,
+                                      G, M_max, N, K, d_staging, staging_bytes, stream=None):
+    _check(load().nvfp4_grouped_gemm_nt_masked_host(
+        _ptr(h_A), _ptr(h_A_sf), _ptr(h_alpha), _ptr(h_masked_m), _ptr(B), _ptr(B_sf),
+        _ptr(h_C), G, M_max, N, K, _ptr(d_staging), staging_bytes, _stream(stream)),
+        "nvfp4_grouped_gemm_nt_masked_host")
+
+
+def nvfp4_gg_set_sm_count(sm_count: int):
+    _check(load().nvfp4_gg_set_sm_count(sm_count), "nvfp4_gg_set_sm_count")
+
+
+def nvfp4_gg_check_error(stream=None) -> int:
+    """Synchronises the stream; returns (and clears) the device error word."""
+    return int(load().nvfp4_gg_check_error(_stream(stream)))
+
+
+def nvfp4_gg_selftest_watchdog(timeout_ns: int, stream=None):
+    _check(load().nvfp4_gg_selftest_watchdog(int(timeout_ns), _stream(stream)),
+           "nvfp4_gg_selftest_watchdog")

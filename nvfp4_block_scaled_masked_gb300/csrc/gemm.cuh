@@ -1,0 +1,444 @@
+// Persistent, warp-specialised tcgen05 kernel for the masked, block-scaled
+// NVFP4 grouped GEMM-NT (FlashInfer's grouped_gemm_nt_masked as described on
+// "The CuteDSL Gamble: Chasing Kernel Efficiency on Blackwell GPUs", "The
+// Message": per expert g and row m < masked_m[g],
+// C[g][m][n] = bf16(alpha[g] * sum_k A[g][m][k] B[g][n][k])).
+//
+// Orientation ("swap-AB"): the MMA's M = 128 rows are weight rows n (B), its
+// N dimension is a tile of tokens m (A) whose width w is chosen per expert at
+// run time (a multiple of 16, up to TT_MAX).  So the weight stream fills the
+// 128-row tensor-core tile even for decode-sized masked_m, and a ragged
+// masked_m wastes at most 15 token columns per tile.
+//
+// Roles (192 threads):
+//   warp 0      TMA producer (one lane): weight tile 128 x 256 codes, its 4
+//               scale atoms (bulk copy), token tile w x 256 codes, and the
+//               token scales (plain rows) into a STAGES-deep shared ring.
+//   warp 1      TMEM owner and MMA issuer: regroups token scales into MMA
+//               atoms (all lanes), copies scale atoms to TMEM (tcgen05.cp),
+//               issues 4 x tcgen05.mma (K = 64 each) per stage from one lane.
+//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (lane = n,
+//               column = token), x alpha[g], bf16 round-to-nearest, stores of
+//               rows m < masked_m[g] only.
+// Tiles are walked persistently: CTA b takes tiles b, b + grid, ...; the
+// tile list holds, per expert in order, ceil(N/128) weight blocks times the
+// token tiles of that expert, and experts with masked_m = 0 contribute none.
+//
+// Scale factors in TMEM: the MMA reads the scale of operand row r from TMEM
+// lane r % 32 (any quarter), column base + r / 32, byte = 16-element K block.
+// A 512-byte "atom" of 32 rows x 16 bytes (row i: rows i, i+32, i+64, i+96 x 4
+// K blocks) copied with tcgen05.cp.32x128b.warpx4 lands exactly there.
+//
+// Every wait on an mbarrier is bounded (time limit in the parameters); on
+// expiry the waiter records NVFP4GG_ERR_TIMEOUT in the error word, raises a
+// shared abort flag that makes the other roles stop, in-flight copies and
+// MMAs are drained with bounded waits, TMEM is freed and the kernel returns.
+#pragma once
+#include <cuda_bf16.h>
+#include "ptx.cuh"
+#include "nvfp4gg.h"
+
+namespace nvfp4gg {
+
+constexpr int kGroupsMax = NVFP4GG_MAX_GROUPS;
+constexpr int kThreads = 192;
+constexpr int kNumBoxes = 5;   // token boxes of 16, 32, 64, 128, 256 rows
+
+struct GemmParams {
+    CUtensorMap tm_w;                // prepared B codes u8 [G][N][K/2], box 128 x 128 rows, SW128
+    CUtensorMap tm_a[kNumBoxes];     // A codes u8 [G][M_max][K/2], box 128 x (16 << i), SW128
+    CUtensorMap tm_asf[kNumBoxes];   // A_sf u8 [G][M_max][K/16], box 16 x (16 << i)
+    const uint8_t* wsf;              // prepared scales: [G][NT][K/64][512]
+    const float* alpha;
+    const int* masked_m;
+    __nv_bfloat16* C;
+    int* err;
+    int G, M_max, N, K, NT, KS;
+    unsigned long long timeout_ns;
+};
+
+__host__ __device__ constexpr int pow2_cols(int n) {
+    return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
+}
+
+template <int TT_MAX, int STAGES>
+struct KCfg {
+    static_assert(TT_MAX % 32 == 0 && TT_MAX <= 256, "token tile");
+    static constexpr int W_TILE = 128 * 128;         // 128 weight rows x 256 codes
+    static constexpr int T_TILE = TT_MAX * 128;      // TT_MAX token rows x 256 codes
+    static constexpr int WSF_STAGE = 4 * 512;        // 4 weight-scale atoms
+    static constexpr int TSF_PLAIN = TT_MAX * 16;    // token scales, 16 bytes per row
+    static constexpr int NA = (TT_MAX + 127) / 128;  // token atoms per MMA
+    static constexpr int JMAX = TT_MAX / 32 < 4 ? TT_MAX / 32 : 4;
+    static constexpr int TSF_ATOMS = 4 * NA * 512;
+    static constexpr int ACC_BUFS = 2;
+    static constexpr int SFW_COLS = 16;              // 4 MMAs x 4 columns
+    static constexpr int SFT_COLS = 16 * NA;
+    static constexpr int SF_COLS = SFW_COLS + SFT_COLS;
+    static constexpr int TMEM_NEED = ACC_BUFS * TT_MAX + STAGES * SF_COLS;
+    static_assert(TMEM_NEED <= 512, "TMEM budget");
+    static constexpr int TMEM_COLS = pow2_cols(TMEM_NEED);
+
+    static constexpr int OFF_W = 0;
+    static constexpr int OFF_T = OFF_W + STAGES * W_TILE;
+    static constexpr int OFF_WSF = OFF_T + STAGES * T_TILE;
+    static constexpr int OFF_TSFP = OFF_WSF + STAGES * WSF_STAGE;
+    static constexpr int OFF_TSFA = OFF_TSFP + STAGES * TSF_PLAIN;
+    static constexpr int OFF_BAR = OFF_TSFA + STAGES * TSF_ATOMS;
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int OFF_TAB = (OFF_MISC + 16 + 15) & ~15;
+    // cum[kGroupsMax + 1], gw[kGroupsMax] (w | ntt << 16), gm[kGroupsMax]
+    static constexpr int TAB_BYTES = (3 * kGroupsMax + 1) * 4;
+    static constexpr int SMEM_BYTES = OFF_TAB + TAB_BYTES + 1024;   // + alignment slack
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+__device__ __forceinline__ void record_error(int* err, int code) {
+    atomicCAS(err, 0, code);
+}
+
+// Bounded wait for the phase of `bar` with parity `parity`.  Gives up when
+// the shared abort flag is raised by another role, or after timeout_ns, in
+// which case it records the timeout and raises the flag itself.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
+                                             volatile int* abort_flag, int* err,
+                                             unsigned long long timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                *abort_flag = 1;
+                record_error(err, NVFP4GG_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+struct TileCoord {
+    int g, nt, t0, w, m;
+};
+
+// Tile id -> (expert, weight block, first token, token width, masked_m).
+__device__ __forceinline__ TileCoord decode_tile(const int* cum, const int* gw, const int* gm,
+                                                 int G, int tile) {
+    int lo = 0, hi = G - 1;   // the last g with cum[g] <= tile
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cum[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    TileCoord c;
+    c.g = lo;
+    const int local = tile - cum[lo];
+    const int x = gw[lo];
+    c.w = x & 0xFFFF;
+    const int ntt = x >> 16;
+    c.nt = local / ntt;
+    c.t0 = (local - c.nt * ntt) * c.w;
+    c.m = gm[lo];
+    return c;
+}
+
+template <int TT_MAX, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
+    using Cfg = KCfg<TT_MAX, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sbase = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const uint32_t bar_full = base + Cfg::OFF_BAR;
+    const uint32_t bar_empty = bar_full + 8 * STAGES;
+    const uint32_t bar_accf = bar_empty + 8 * STAGES;
+    const uint32_t bar_acce = bar_accf + 8 * Cfg::ACC_BUFS;
+    const uint32_t bar_done = bar_acce + 8 * Cfg::ACC_BUFS;
+    uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Cfg::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+    int* cum = reinterpret_cast<int*>(sbase + Cfg::OFF_TAB);
+    int* gw = cum + kGroupsMax + 1;
+    int* gm = gw + kGroupsMax;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < Cfg::ACC_BUFS; ++b) {
+            mbar_init(bar_accf + 8 * b, 1);
+            mbar_init(bar_acce + 8 * b, 4);
+        }
+        mbar_init(bar_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(base + Cfg::OFF_MISC, Cfg::TMEM_COLS);
+        tmem_relinquish();   // this CTA allocates nothing else: let others allocate
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&p.tm_w);
+        for (int i = 0; i < kNumBoxes; ++i) {
+            prefetch_tmap(&p.tm_a[i]);
+            prefetch_tmap(&p.tm_asf[i]);
+        }
+    }
+
+    // Per-expert tables: valid rows, token tiles, token width; then the
+    // exclusive prefix of tile counts (ntt * NT per expert).
+    for (int g = threadIdx.x; g < p.G; g += kThreads) {
+        int m = __ldg(p.masked_m + g);
+        if (m < 0 || m > p.M_max) {
+            record_error(p.err, NVFP4GG_ERR_MASK);
+            m = m < 0 ? 0 : p.M_max;
+        }
+        const int ntt = (m + TT_MAX - 1) / TT_MAX;
+        const int w = ntt ? (((m + ntt - 1) / ntt + 15) & ~15) : 0;
+        gw[g] = w | (ntt << 16);
+        gm[g] = m;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int per = (p.G + 31) / 32;
+        const int lo = lane * per;
+        const int hi = min(p.G, lo + per);
+        int sum = 0;
+        for (int g = lo; g < hi; ++g) sum += (gw[g] >> 16) * p.NT;
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        int run = incl - sum;
+        for (int g = lo; g < hi; ++g) {
+            cum[g] = run;
+            run += (gw[g] >> 16) * p.NT;
+        }
+        if (lane == 31) cum[p.G] = incl;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const int total = cum[p.G];
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_stream = policy_evict_first();
+            int s = 0;
+            uint32_t ph = 0;
+            long long issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const TileCoord tc = decode_tile(cum, gw, gm, p.G, tile);
+                const uint8_t* wsf_tile =
+                    p.wsf + ((size_t)tc.g * p.NT + tc.nt) * (size_t)p.KS * Cfg::WSF_STAGE;
+                for (int ks = 0; ks < p.KS; ++ks) {
+                    if (!wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort_flag, p.err, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = bar_full + 8 * s;
+                    mbar_arrive_expect_tx(fb, Cfg::W_TILE + Cfg::WSF_STAGE + tc.w * (128 + 16));
+                    tma_load_3d_hint(base + Cfg::OFF_W + s * Cfg::W_TILE, &p.tm_w, fb, ks * 128,
+                                     tc.nt * 128, tc.g, pol_stream);
+                    bulk_load_hint(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE,
+                                   wsf_tile + (size_t)ks * Cfg::WSF_STAGE, Cfg::WSF_STAGE, fb,
+                                   pol_stream);
+                    int r = 0;
+#pragma unroll
+                    for (int i = kNumBoxes - 1; i >= 0; --i) {
+                        if ((16 << i) > TT_MAX) continue;
+                        if ((tc.w >> 4) & (1 << i)) {
+                            tma_load_3d(base + Cfg::OFF_T + s * Cfg::T_TILE + r * 128, &p.tm_a[i], fb,
+                                        ks * 128, tc.t0 + r, tc.g);
+                            tma_load_3d(base + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN + r * 16,
+                                        &p.tm_asf[i], fb, ks * 16, tc.t0 + r, tc.g);
+                            r += 16 << i;
+                        }
+                    }
+                    ++issued;
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+            }
+            // Drain: every stage's last issued load must have landed before
+            // the CTA may exit (normally already consumed; bounded on abort).
+            for (int st = 0; st < STAGES; ++st) {
+                if (st >= issued) break;
+                const long long last = st + (long long)STAGES * ((issued - 1 - st) / STAGES);
+                const uint32_t par = (uint32_t)((last / STAGES) & 1);
+                volatile int no_abort = 0;
+                wait_bounded(bar_full + 8 * st, par, &no_abort, p.err, p.timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        int s = 0;
+        uint32_t ph = 0;
+        int acc = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            const TileCoord tc = decode_tile(cum, gw, gm, p.G, tile);
+            ok = __all_sync(0xffffffffu, wait_bounded(bar_acce + 8 * acc, aph ^ 1u, abort_flag,
+                                                      p.err, p.timeout_ns));
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t idesc = idesc_mxf4nvf4((uint32_t)tc.w);
+            const uint32_t d_tmem = tmem + acc * TT_MAX;
+            for (int ks = 0; ks < p.KS; ++ks) {
+                ok = __all_sync(0xffffffffu,
+                                wait_bounded(bar_full + 8 * s, ph, abort_flag, p.err, p.timeout_ns));
+                if (!ok) break;
+                // Token scales: plain rows (token t: 4 words, one per MMA) ->
+                // per-MMA atoms (row i: tokens i, i+32, i+64, i+96).
+                {
+                    const uint8_t* plain = sbase + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN;
+                    uint8_t* atoms = sbase + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
+#pragma unroll
+                    for (int a = 0; a < Cfg::NA; ++a) {
+                        uint4 v[4] = {};
+#pragma unroll
+                        for (int j = 0; j < Cfg::JMAX; ++j)
+                            v[j] = *reinterpret_cast<const uint4*>(plain + (128 * a + 32 * j + lane) * 16);
+                        *reinterpret_cast<uint4*>(atoms + (0 * Cfg::NA + a) * 512 + lane * 16) =
+                            make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+                        *reinterpret_cast<uint4*>(atoms + (1 * Cfg::NA + a) * 512 + lane * 16) =
+                            make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
+                        *reinterpret_cast<uint4*>(atoms + (2 * Cfg::NA + a) * 512 + lane * 16) =
+                            make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
+                        *reinterpret_cast<uint4*>(atoms + (3 * Cfg::NA + a) * 512 + lane * 16) =
+                            make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
+                    }
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tc_fence_after();
+                    const uint32_t sfw = tmem + Cfg::ACC_BUFS * TT_MAX + s * Cfg::SF_COLS;
+                    const uint32_t sft = sfw + Cfg::SFW_COLS;
+                    const uint32_t wsf_s = base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE;
+                    const uint32_t tsfa_s = base + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) tmem_cp_32x128b_x4(sfw + 4 * q, sdesc_rows16(wsf_s + 512 * q));
+#pragma unroll
+                    for (int q = 0; q < 4 * Cfg::NA; ++q)
+                        tmem_cp_32x128b_x4(sft + 4 * q, sdesc_rows16(tsfa_s + 512 * q));
+                    const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_W + s * Cfg::W_TILE);
+                    const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_T + s * Cfg::T_TILE);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        umma_mxf4nvf4(d_tmem, ad + 2 * q, bd + 2 * q, idesc, sfw + 4 * q,
+                                      sft + 4 * Cfg::NA * q, (ks | q) != 0);
+                    umma_commit(bar_empty + 8 * s);
+                    if (ks == p.KS - 1) umma_commit(bar_accf + 8 * acc);
+                }
+                __syncwarp();
+                if (++s == STAGES) { s = 0; ph ^= 1u; }
+            }
+            if (++acc == Cfg::ACC_BUFS) { acc = 0; aph ^= 1u; }
+        }
+        // Drain the tensor pipe before TMEM is freed.
+        if (lane == 0) umma_commit(bar_done);
+        __syncwarp();
+        volatile int no_abort = 0;
+        wait_bounded(bar_done, 0, &no_abort, p.err, p.timeout_ns);
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quad = warp & 3;   // TMEM lane quarter this warp may access
+        int acc = 0;
+        uint32_t aph = 0;
+        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const TileCoord tc = decode_tile(cum, gw, gm, p.G, tile);
+            const bool ok = __all_sync(0xffffffffu, wait_bounded(bar_accf + 8 * acc, aph, abort_flag,
+                                                                 p.err, p.timeout_ns));
+            if (!ok) break;
+            tc_fence_after();
+            const float al = __ldg(p.alpha + tc.g);
+            const int n = tc.nt * 128 + quad * 32 + lane;
+            const int t_end = min(tc.t0 + tc.w, tc.m);
+            const uint32_t tbase = tmem + acc * TT_MAX + ((uint32_t)(quad * 32) << 16);
+            __nv_bfloat16* crow = p.C + ((size_t)tc.g * p.M_max) * p.N + n;
+#pragma unroll 1
+            for (int c = 0; c < TT_MAX / 16; ++c) {
+                if (c * 16 >= tc.w) break;
+                uint32_t r[16];
+                tmem_ld_32x32b_x16(tbase + c * 16, r);
+                tmem_wait_ld();
+                if (n < p.N) {
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const int tok = tc.t0 + c * 16 + t;
+                        if (tok < t_end)
+                            crow[(size_t)tok * p.N] = __float2bfloat16_rn(al * __uint_as_float(r[t]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_acce + 8 * acc);
+            if (++acc == Cfg::ACC_BUFS) { acc = 0; aph ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    }
+}
+
+// One CTA waits on a barrier that nothing completes; the bounded wait gives
+// up after timeout_ns and records NVFP4GG_ERR_TIMEOUT.
+__global__ void watchdog_selftest_kernel(int* err, unsigned long long timeout_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        wait_bounded(smem_u32(&bar), 0, &abort_flag, err, timeout_ns);
+    __syncthreads();
+}
+
+// Weight-scale re-layout: B_sf u8 [G][N][K/16] -> atoms [G][NT][K/64][32][4][4]
+// where atom byte (i, j, b) is the scale of row 128*nt + 32*j + i, K block
+// 4*kc + b (zero for rows >= N).  One thread per 16-byte atom row.
+__global__ void relayout_weight_scales_kernel(const uint8_t* __restrict__ bsf,
+                                              uint8_t* __restrict__ out, int G, int N, int K) {
+    const int NT = (N + 127) / 128;
+    const int KC = K / 64;
+    const long long rows = (long long)G * NT * KC * 32;
+    const int ks16 = K / 16;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < rows;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int i = (int)(idx & 31);
+        long long rest = idx >> 5;
+        const int kc = (int)(rest % KC);
+        rest /= KC;
+        const int nt = (int)(rest % NT);
+        const int g = (int)(rest / NT);
+        uint32_t wv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = nt * 128 + 32 * j + i;
+            wv[j] = n < N ? *reinterpret_cast<const uint32_t*>(bsf + ((size_t)g * N + n) * ks16 + 4 * kc)
+                          : 0u;
+        }
+        *reinterpret_cast<uint4*>(out + idx * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
+}
+
+}  // namespace nvfp4gg

@@ -1,0 +1,299 @@
+// C-ABI of libnvfp4gg: argument checks, tensor-map set-up and kernel launch
+// for the masked, block-scaled NVFP4 grouped GEMM-NT (include/nvfp4gg.h).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "gemm.cuh"
+#include "nvfp4gg.h"
+
+using namespace nvfp4gg;
+
+// Device error word (one per device that loads the library).
+static __device__ int g_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int status = NVFP4GG_OK;
+    int sms = 0;
+    int* err = nullptr;          // device address of g_error_word
+    bool attr_set[8] = {};       // per kernel variant: max dynamic smem set
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+int g_sm_cap = 0;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+unsigned long long g_timeout_ns = 2000000000ull;   // 2 s per device-side wait
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4GG_OK : NVFP4GG_ERR_CUDA; }
+
+// Per-device one-time set-up: architecture check, SM count, error word.
+int device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4GG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            return NVFP4GG_ERR_CUDA;
+        }
+        if (major != 10 || minor != 3) {
+            d.status = NVFP4GG_ERR_ARCH;
+        } else if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.err), g_error_word) != cudaSuccess) {
+            return NVFP4GG_ERR_CUDA;
+        }
+        if (!g_encode) {
+            void* fn = nullptr;
+            cudaDriverEntryPointQueryResult q;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || !fn) {
+                return NVFP4GG_ERR_CUDA;
+            }
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    if (d.status != NVFP4GG_OK) return d.status;
+    *out = &d;
+    return NVFP4GG_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// 3-D u8 tensor map: dims (d0 innermost bytes, d1 rows, d2 groups).
+int encode_u8_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint64_t d2,
+                 uint32_t box0, uint32_t box1, CUtensorMapSwizzle swz) {
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0, d0 * d1};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(ptr), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? NVFP4GG_OK : NVFP4GG_ERR_CUDA;
+}
+
+int check_gemm_shape(int G, int M_max, int N, int K) {
+    if (G < 1 || G > NVFP4GG_MAX_GROUPS) return NVFP4GG_ERR_SHAPE;
+    if (M_max < 1 || M_max > (1 << 20)) return NVFP4GG_ERR_SHAPE;
+    if (N < NVFP4GG_N_ALIGN || N % NVFP4GG_N_ALIGN != 0 || N > (1 << 20)) return NVFP4GG_ERR_SHAPE;
+    if (K < NVFP4GG_K_ALIGN || K % NVFP4GG_K_ALIGN != 0 || K > (1 << 20)) return NVFP4GG_ERR_SHAPE;
+    return NVFP4GG_OK;
+}
+
+template <int TT, int ST>
+int launch_variant(DeviceState* d, int slot, const GemmParams& p, cudaStream_t stream) {
+    using Cfg = KCfg<TT, ST>;
+    auto kern = gemm_nt_masked_kernel<TT, ST>;
+    if (!d->attr_set[slot]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM_BYTES) != cudaSuccess)
+            return NVFP4GG_ERR_CUDA;
+        d->attr_set[slot] = true;
+    }
+    int grid = d->sms;
+    if (g_sm_cap > 0 && g_sm_cap < grid) grid = g_sm_cap;
+    kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(p);
+    return cuda_status(cudaGetLastError());
+}
+
+// Decode-sized experts (M_max <= 64): token tiles of at most 32, a deep ring
+// for the weight stream.  Larger experts: token tiles of up to 128.
+constexpr int kNarrowTT = 32, kNarrowStages = 8;
+constexpr int kWideTT = 128, kWideStages = 5;
+
+}  // namespace
+
+extern "C" {
+
+const char* nvfp4_gg_status_string(int s) {
+    switch (s) {
+        case NVFP4GG_OK: return "NVFP4GG_OK";
+        case NVFP4GG_ERR_NULL: return "NVFP4GG_ERR_NULL: a required pointer is NULL";
+        case NVFP4GG_ERR_SHAPE: return "NVFP4GG_ERR_SHAPE: unsupported G, M_max, N or K";
+        case NVFP4GG_ERR_ALIGN: return "NVFP4GG_ERR_ALIGN: pointer not aligned as required";
+        case NVFP4GG_ERR_ARCH: return "NVFP4GG_ERR_ARCH: device is not compute capability 10.3";
+        case NVFP4GG_ERR_CUDA: return "NVFP4GG_ERR_CUDA: a CUDA call failed";
+        case NVFP4GG_ERR_TIMEOUT: return "NVFP4GG_ERR_TIMEOUT: a device-side wait ran out";
+        case NVFP4GG_ERR_MASK: return "NVFP4GG_ERR_MASK: masked_m outside [0, M_max]";
+        default: return "unknown nvfp4gg status";
+    }
+}
+
+int nvfp4_prepared_weight_bytes(int G, int N, int K, size_t* b_bytes, size_t* sf_bytes) {
+    if (!b_bytes || !sf_bytes) return NVFP4GG_ERR_NULL;
+    if (G < 1 || G > NVFP4GG_MAX_GROUPS || N < NVFP4GG_N_ALIGN || N % NVFP4GG_N_ALIGN ||
+        N > (1 << 20) || K < NVFP4GG_K_ALIGN || K % NVFP4GG_K_ALIGN || K > (1 << 20))
+        return NVFP4GG_ERR_SHAPE;
+    *b_bytes = (size_t)G * N * (K / 2);
+    *sf_bytes = (size_t)G * ((N + 127) / 128) * (K / 64) * 512;
+    return NVFP4GG_OK;
+}
+
+int nvfp4_prepare_weights(const void* B, const void* B_sf, int G, int N, int K, void* B_prep,
+                          void* B_sf_prep, void* stream) {
+    if (!B || !B_sf || !B_prep || !B_sf_prep) return NVFP4GG_ERR_NULL;
+    size_t bb = 0, sb = 0;
+    int rc = nvfp4_prepared_weight_bytes(G, N, K, &bb, &sb);
+    if (rc != NVFP4GG_OK) return rc;
+    if (!aligned(B, 16) || !aligned(B_sf, 16) || !aligned(B_prep, 16) || !aligned(B_sf_prep, 16))
+        return NVFP4GG_ERR_ALIGN;
+    if (B_sf == B_sf_prep) return NVFP4GG_ERR_SHAPE;
+    DeviceState* d = nullptr;
+    if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (B_prep != B) {
+        if (cudaMemcpyAsync(B_prep, B, bb, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return NVFP4GG_ERR_CUDA;
+    }
+    const long long rows = (long long)(sb / 16);
+    const int threads = 256;
+    long long blocks = (rows + threads - 1) / threads;
+    if (blocks > 16LL * d->sms) blocks = 16LL * d->sms;
+    relayout_weight_scales_kernel<<<(int)blocks, threads, 0, st>>>(
+        static_cast<const uint8_t*>(B_sf), static_cast<uint8_t*>(B_sf_prep), G, N, K);
+    return cuda_status(cudaGetLastError());
+}
+
+int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B, const void* B_sf,
+                                 const float* alpha, const int* masked_m, void* C, int G, int M_max,
+                                 int N, int K, void* stream) {
+    if (!A || !A_sf || !B || !B_sf || !alpha || !masked_m || !C) return NVFP4GG_ERR_NULL;
+    int rc = check_gemm_shape(G, M_max, N, K);
+    if (rc != NVFP4GG_OK) return rc;
+    if (!aligned(A, 16) || !aligned(A_sf, 16) || !aligned(B, 16) || !aligned(B_sf, 16) ||
+        !aligned(C, 16) || !aligned(alpha, 4) || !aligned(masked_m, 4))
+        return NVFP4GG_ERR_ALIGN;
+    DeviceState* d = nullptr;
+    if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
+
+    const bool narrow = M_max <= 64;
+    const int tt_max = narrow ? kNarrowTT : kWideTT;
+    GemmParams p;
+    std::memset(&p, 0, sizeof(p));
+    const uint64_t kb = (uint64_t)K / 2, ks = (uint64_t)K / 16;
+    if ((rc = encode_u8_3d(&p.tm_w, B, kb, N, G, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != NVFP4GG_OK)
+        return rc;
+    // token boxes of 16 << i rows; boxes that no tile can use repeat the 16-row map
+    const int rows_cap = ((M_max + 15) / 16) * 16;
+    for (int i = 0; i < kNumBoxes; ++i) {
+        const uint32_t box = 16u << i;
+        const uint32_t b = (box <= (uint32_t)tt_max && box <= (uint32_t)rows_cap) ? box : 16u;
+        if ((rc = encode_u8_3d(&p.tm_a[i], A, kb, M_max, G, 128, b, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+            NVFP4GG_OK)
+            return rc;
+        if ((rc = encode_u8_3d(&p.tm_asf[i], A_sf, ks, M_max, G, 16, b, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
+            NVFP4GG_OK)
+            return rc;
+    }
+    p.wsf = static_cast<const uint8_t*>(B_sf);
+    p.alpha = alpha;
+    p.masked_m = masked_m;
+    p.C = static_cast<__nv_bfloat16*>(C);
+    p.err = d->err;
+    p.G = G;
+    p.M_max = M_max;
+    p.N = N;
+    p.K = K;
+    p.NT = (N + 127) / 128;
+    p.KS = K / 256;
+    p.timeout_ns = g_timeout_ns;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (narrow) return launch_variant<kNarrowTT, kNarrowStages>(d, 0, p, st);
+    return launch_variant<kWideTT, kWideStages>(d, 1, p, st);
+}
+
+size_t nvfp4_host_staging_bytes(int G, int M_max, int N, int K) {
+    if (check_gemm_shape(G, M_max, N, K) != NVFP4GG_OK) return 0;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    return up((size_t)G * M_max * N * 2) + up((size_t)G * M_max * (K / 2)) +
+           up((size_t)G * M_max * (K / 16)) + up((size_t)G * 4) + up((size_t)G * 4);
+}
+
+int nvfp4_grouped_gemm_nt_masked_host(const void* h_A, const void* h_A_sf, const float* h_alpha,
+                                      const int* h_masked_m, const void* B, const void* B_sf,
+                                      void* h_C, int G, int M_max, int N, int K, void* d_staging,
+                                      size_t staging_bytes, void* stream) {
+    if (!h_A || !h_A_sf || !h_alpha || !h_masked_m || !B || !B_sf || !h_C || !d_staging)
+        return NVFP4GG_ERR_NULL;
+    int rc = check_gemm_shape(G, M_max, N, K);
+    if (rc != NVFP4GG_OK) return rc;
+    if (staging_bytes < nvfp4_host_staging_bytes(G, M_max, N, K)) return NVFP4GG_ERR_SHAPE;
+    if (!aligned(d_staging, 16)) return NVFP4GG_ERR_ALIGN;
+    for (int g = 0; g < G; ++g)
+        if (h_masked_m[g] < 0 || h_masked_m[g] > M_max) return NVFP4GG_ERR_SHAPE;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    const size_t c_bytes = (size_t)G * M_max * N * 2;
+    const size_t a_bytes = (size_t)G * M_max * (K / 2);
+    const size_t asf_bytes = (size_t)G * M_max * (K / 16);
+    uint8_t* dC = static_cast<uint8_t*>(d_staging);
+    uint8_t* dA = dC + up(c_bytes);
+    uint8_t* dAsf = dA + up(a_bytes);
+    float* dAlpha = reinterpret_cast<float*>(dAsf + up(asf_bytes));
+    int* dMask = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(dAlpha) + up((size_t)G * 4));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(dA, h_A, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(dAsf, h_A_sf, asf_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(dAlpha, h_alpha, (size_t)G * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+        cudaMemcpyAsync(dMask, h_masked_m, (size_t)G * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return NVFP4GG_ERR_CUDA;
+    rc = nvfp4_grouped_gemm_nt_masked(dA, dAsf, B, B_sf, dAlpha, dMask, dC, G, M_max, N, K, stream);
+    if (rc != NVFP4GG_OK) return rc;
+    const size_t group_bytes = (size_t)M_max * N * 2;
+    for (int g = 0; g < G; ++g) {
+        if (h_masked_m[g] == 0) continue;
+        if (cudaMemcpyAsync(static_cast<uint8_t*>(h_C) + g * group_bytes, dC + g * group_bytes,
+                            (size_t)h_masked_m[g] * N * 2, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+            return NVFP4GG_ERR_CUDA;
+    }
+    return NVFP4GG_OK;
+}
+
+int nvfp4_gg_set_sm_count(int sm_count) {
+    if (sm_count < 0) return NVFP4GG_ERR_SHAPE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_sm_cap = sm_count;
+    return NVFP4GG_OK;
+}
+
+int nvfp4_gg_check_error(void* stream) {
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != NVFP4GG_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return NVFP4GG_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, d->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return NVFP4GG_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(d->err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+            return NVFP4GG_ERR_CUDA;
+    }
+    return word;
+}
+
+int nvfp4_gg_selftest_watchdog(long long timeout_ns, void* stream) {
+    if (timeout_ns < 1000 || timeout_ns > 10000000000LL) return NVFP4GG_ERR_SHAPE;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != NVFP4GG_OK) return rc;
+    watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        d->err, (unsigned long long)timeout_ns);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // extern "C"

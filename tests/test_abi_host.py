@@ -1,0 +1,111 @@
+"""Host-side checks of the C-ABI library: it builds for sm_103a, loads, exports
+every entry point include/nvfp4gg.h declares, and rejects bad arguments with
+the documented status before touching the GPU (no GPU needed)."""
+import os
+import re
+
+import pytest
+
+from nvfp4_block_scaled_masked_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "nvfp4gg.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in nvfp4gg.h but not exported"
+    assert sorted(binding.EXPORTS) == names
+
+
+def test_status_strings(lib):
+    for s in range(0, -8, -1):
+        assert binding.status_string(s).startswith("NVFP4GG_")
+    assert "unknown" in binding.status_string(42)
+
+
+def test_prepared_weight_bytes(lib):
+    b, s = binding.nvfp4_prepared_weight_bytes(32, 4096, 7168)
+    assert b == 32 * 4096 * 3584
+    assert s == 32 * 32 * (7168 // 64) * 512 == 32 * 4096 * 7168 // 16
+    b, s = binding.nvfp4_prepared_weight_bytes(2, 144, 512)   # N tail padded to 256 rows
+    assert s == 2 * 2 * 8 * 512
+    for bad in [(0, 128, 256), (1025, 128, 256), (1, 120, 256), (1, 128, 320), (1, 128, 0)]:
+        with pytest.raises(binding.NVFP4GGError) as e:
+            binding.nvfp4_prepared_weight_bytes(*bad)
+        assert e.value.status == binding.ERR_SHAPE
+
+
+FAKE = 0x10000   # aligned, never dereferenced: every call below fails its checks first
+
+
+def gemm(lib, A=FAKE, A_sf=FAKE, B=FAKE, B_sf=FAKE, alpha=FAKE, mask=FAKE, C=FAKE,
+         G=4, M=16, N=256, K=256):
+    return lib.nvfp4_grouped_gemm_nt_masked(A, A_sf, B, B_sf, alpha, mask, C, G, M, N, K, None)
+
+
+@pytest.mark.parametrize("field", ["A", "A_sf", "B", "B_sf", "alpha", "mask", "C"])
+def test_null_pointers_rejected(lib, field):
+    assert gemm(lib, **{field: None}) == binding.ERR_NULL
+
+
+@pytest.mark.parametrize("shape", [
+    dict(G=0), dict(G=1025), dict(M=0), dict(N=0), dict(N=8), dict(N=136),
+    dict(K=0), dict(K=128), dict(K=320), dict(G=-3),
+])
+def test_bad_shapes_rejected(lib, shape):
+    assert gemm(lib, **shape) == binding.ERR_SHAPE
+
+
+@pytest.mark.parametrize("field,addr", [("A", FAKE + 8), ("A_sf", FAKE + 4), ("B", FAKE + 1),
+                                        ("B_sf", FAKE + 2), ("C", FAKE + 2),
+                                        ("alpha", FAKE + 2), ("mask", FAKE + 1)])
+def test_misaligned_pointers_rejected(lib, field, addr):
+    assert gemm(lib, **{field: addr}) == binding.ERR_ALIGN
+
+
+def test_prepare_weights_argument_checks(lib):
+    f = lib.nvfp4_prepare_weights
+    assert f(None, FAKE, 1, 128, 256, FAKE, FAKE + 4096, None) == binding.ERR_NULL
+    assert f(FAKE, FAKE, 1, 100, 256, FAKE, FAKE + 4096, None) == binding.ERR_SHAPE
+    assert f(FAKE + 1, FAKE, 1, 128, 256, FAKE, FAKE + 4096, None) == binding.ERR_ALIGN
+    assert f(FAKE, FAKE, 1, 128, 256, FAKE, FAKE, None) == binding.ERR_SHAPE   # scales in place
+
+
+def test_host_variant_argument_checks(lib):
+    need = binding.nvfp4_host_staging_bytes(4, 16, 256, 256)
+    up = lambda x: (x + 255) // 256 * 256
+    assert need == up(4 * 16 * 256 * 2) + up(4 * 16 * 128) + up(4 * 16 * 16) + 2 * up(16)
+    assert binding.nvfp4_host_staging_bytes(0, 16, 256, 256) == 0
+    f = lib.nvfp4_grouped_gemm_nt_masked_host
+    args = [FAKE] * 7 + [4, 16, 256, 256, FAKE, need, None]
+    a = list(args); a[0] = None
+    assert f(*a) == binding.ERR_NULL
+    a = list(args); a[12] = need - 1
+    assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[11] = FAKE + 8
+    assert f(*a) == binding.ERR_ALIGN
+
+
+def test_sm_cap_and_watchdog_argument_checks(lib):
+    assert lib.nvfp4_gg_set_sm_count(-1) == binding.ERR_SHAPE
+    assert lib.nvfp4_gg_set_sm_count(0) == binding.OK
+    assert lib.nvfp4_gg_selftest_watchdog(10, None) == binding.ERR_SHAPE
+    assert lib.nvfp4_gg_selftest_watchdog(10 ** 11, None) == binding.ERR_SHAPE
+
+
+def test_library_targets_sm103a_only():
+    assert build.ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]

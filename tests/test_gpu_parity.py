@@ -1,0 +1,184 @@
+"""GPU parity: the CUDA path against the CPU oracle, element by element.
+
+Bar (the stated acceptance test): for every valid (g, m, n),
+|gpu - ref| <= 4e-3 |ref| + 1e-4 max|ref|, ref the oracle's unrounded fp64
+value and max taken over the call; rows m >= masked_m[g] bit-identical to the
+0x7FC0 prefill.  Calls go through the C-ABI (ctypes binding)."""
+import numpy as np
+import pytest
+
+from oracle import oracle
+from nvfp4_block_scaled_masked_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from nvfp4_block_scaled_masked_gb300 import build, binding
+    build.build()
+    binding.load()
+    assert binding.nvfp4_gg_check_error() == 0
+    return binding
+
+
+def bf16_to_f64(bits):
+    return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def run_gpu(d):
+    from nvfp4_block_scaled_masked_gb300.device import Problem
+    from nvfp4_block_scaled_masked_gb300 import binding
+    prob = Problem(d)
+    prob.run()
+    rc = binding.nvfp4_gg_check_error()
+    assert rc == 0, binding.status_string(rc)
+    return prob.C_bits()
+
+
+def check_full(d, C_gpu):
+    cfg = d["cfg"]
+    C_ref, ref = oracle.gemm(d["A"], d["A_sf"], d["B"], d["B_sf"], d["alpha"], d["masked_m"],
+                             d["C_init"], cfg.G, cfg.M_max, cfg.N, cfg.K)
+    mm = d["masked_m"]
+    valid = np.zeros((cfg.G, cfg.M_max), dtype=bool)
+    for g in range(cfg.G):
+        valid[g, :mm[g]] = True
+    # invariants: untouched rows bit-identical to the prefill
+    assert np.all(C_gpu[~valid] == W.SENTINEL_BF16), "rows >= masked_m were written"
+    if not valid.any():
+        return
+    vals = bf16_to_f64(C_gpu[valid])
+    r = ref[valid]
+    assert np.all(np.isfinite(vals))
+    max_abs = np.abs(r).max()
+    ok = oracle.tolerance_ok(vals, r, max_abs)
+    if not ok.all():
+        bad = np.flatnonzero(~ok.ravel())
+        idx = np.argwhere(valid)
+        cols = bad % cfg.N
+        rows = idx[bad // cfg.N]
+        msg = [f"{len(bad)} of {ok.size} outside tolerance; first:"]
+        for b, (g, m), n in list(zip(bad, rows, cols))[:8]:
+            msg.append(f"  g={g} m={m} n={n} gpu={vals.ravel()[b]!r} ref={r.ravel()[b]!r}")
+        pytest.fail("\n".join(msg))
+    # most values should be the correctly rounded bf16 (fp32 accumulation order
+    # only rarely moves a value across a rounding boundary)
+    same = np.mean(C_gpu[valid] == C_ref[valid])
+    assert same > 0.9, f"only {same:.3f} bit-identical to the correctly rounded oracle"
+
+
+def check_sampled(d, C_gpu, rows_per_group=6, cols=96, seed=0):
+    """Every non-empty expert: its first and last valid row plus random rows,
+    each at `cols` random n; fp64 sampled oracle.  Invariants checked in full."""
+    cfg = d["cfg"]
+    mm = d["masked_m"]
+    for g in range(cfg.G):
+        assert np.all(C_gpu[g, mm[g]:] == W.SENTINEL_BF16), f"expert {g}: rows >= masked_m written"
+    rng = np.random.default_rng(seed)
+    idx = []
+    for g in range(cfg.G):
+        if mm[g] == 0:
+            continue
+        rows = {0, mm[g] - 1} | set(rng.integers(0, mm[g], rows_per_group).tolist())
+        for m in rows:
+            for n in rng.choice(cfg.N, size=min(cols, cfg.N), replace=False):
+                idx.append((g, m, n))
+    idx = np.array(idx, dtype=np.int64)
+    ref = oracle.gemm_sampled(d["A"], d["A_sf"], d["B"], d["B_sf"], d["alpha"], idx,
+                              cfg.G, cfg.M_max, cfg.N, cfg.K)
+    vals = bf16_to_f64(C_gpu[idx[:, 0], idx[:, 1], idx[:, 2]])
+    max_abs = np.abs(ref).max()
+    ok = oracle.tolerance_ok(vals, ref, max_abs)
+    assert ok.all(), (f"{(~ok).sum()} of {ok.size} sampled outputs outside tolerance; "
+                      f"first {idx[~ok][:4].tolist()} gpu={vals[~ok][:4]} ref={ref[~ok][:4]}")
+
+
+def test_c1_small_masked(lib):
+    d = W.generate(W.CONFIGS["c1"])
+    check_full(d, run_gpu(d))
+
+
+def test_c1_poisoned_rows_ignored(lib):
+    d = W.generate(W.CONFIGS["c1"], poison=True)
+    check_full(d, run_gpu(d))
+
+
+@pytest.mark.parametrize("G,M_max,N,K,masked", [
+    (3, 16, 128, 256, [1, 16, 0]),                          # one stage, narrow tiles
+    (5, 40, 144, 512, [40, 33, 32, 17, 0]),                 # N tail, 2 token tiles, 2 stages
+    (2, 64, 256, 1024, [64, 31]),                           # narrow kernel, M_max = 64
+    (4, 200, 272, 768, [200, 129, 128, 1]),                 # wide kernel, ragged widths
+    (2, 256, 384, 512, [256, 255]),                         # wide kernel, 2 x 128 tiles
+    (1, 1, 16, 256, [1]),                                   # minimum sizes
+    (6, 24, 128, 256, [0, 0, 0, 0, 0, 0]),                  # every expert empty
+])
+def test_shapes_ragged_and_edges(lib, G, M_max, N, K, masked):
+    d = W.generate(W.custom(G, M_max, N, K, masked_m=masked), seed=G * 1000 + N)
+    check_full(d, run_gpu(d))
+
+
+def test_c2_decode_full(lib):
+    d = W.generate(W.CONFIGS["c2"])
+    check_full(d, run_gpu(d))
+
+
+@pytest.mark.parametrize("key", ["c3", "c4", "c5"])
+def test_full_size_sampled(lib, key):
+    d = W.generate(W.CONFIGS[key])
+    check_sampled(d, run_gpu(d))
+
+
+def test_alpha_power_of_two_linearity_on_gpu(lib):
+    d = W.generate(W.CONFIGS["c1"])
+    C1 = run_gpu(d)
+    d2 = dict(d)
+    d2["alpha"] = (d["alpha"] * np.float32(0.25)).astype(np.float32)
+    C2 = run_gpu(d2)
+    mm = d["masked_m"]
+    for g in range(len(mm)):
+        np.testing.assert_array_equal(bf16_to_f64(C2[g, :mm[g]]), bf16_to_f64(C1[g, :mm[g]]) * 0.25)
+
+
+def test_watchdog_reports_timeout(lib):
+    lib.nvfp4_gg_selftest_watchdog(2_000_000)      # 2 ms limit on a barrier nobody completes
+    assert lib.nvfp4_gg_check_error() == lib.ERR_TIMEOUT
+    assert lib.nvfp4_gg_check_error() == 0          # the word was cleared
+    d = W.generate(W.CONFIGS["c1"])                 # the context is still usable
+    check_full(d, run_gpu(d))
+
+
+def test_masked_m_out_of_range_is_flagged(lib):
+    from nvfp4_block_scaled_masked_gb300.device import Problem
+    d = W.generate(W.custom(2, 16, 128, 256, masked_m=[16, 3]))
+    prob = Problem(d)
+    prob.masked_m.copy_(torch.tensor([17, 3], dtype=torch.int32))
+    prob.run()
+    assert lib.nvfp4_gg_check_error() == lib.ERR_MASK
+    # clamped to M_max: the result equals the masked_m = [16, 3] result
+    check_full(d, prob.C_bits())
+
+
+def test_prepare_weights_roundtrip(lib):
+    """Re-layout, then the inverse permutation on the CPU, gives back B_sf."""
+    from nvfp4_block_scaled_masked_gb300 import binding
+    G, N, K = 3, 272, 512
+    rng = np.random.default_rng(4)
+    bsf = rng.integers(0, 256, (G, N, K // 16), dtype=np.uint8)
+    b = rng.integers(0, 256, (G, N, K // 2), dtype=np.uint8)
+    bb, sb = binding.nvfp4_prepared_weight_bytes(G, N, K)
+    dB, dBsf = torch.from_numpy(b).cuda(), torch.from_numpy(bsf).cuda()
+    oB = torch.empty(bb, dtype=torch.uint8, device="cuda")
+    oS = torch.empty(sb, dtype=torch.uint8, device="cuda")
+    binding.nvfp4_prepare_weights(dB, dBsf, G, N, K, oB, oS)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(oB.cpu().numpy(), b.ravel())
+    NT, KC = (N + 127) // 128, K // 64
+    atoms = oS.cpu().numpy().reshape(G, NT, KC, 32, 4, 4)      # [g][nt][kc][i][j][b]
+    back = atoms.transpose(0, 1, 4, 3, 2, 5).reshape(G, NT * 128, KC * 4)   # row = 128nt+32j+i
+    np.testing.assert_array_equal(back[:, :N], bsf)
+    assert np.all(back[:, N:] == 0)
