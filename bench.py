@@ -1,0 +1,413 @@
+"""Benchmark of the masked, block-scaled NVFP4 grouped GEMM-NT on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl ours|reference]
+
+One step = one call of nvfp4_grouped_gemm_nt_masked over one batch of the
+synthetic workload (default: the decode GEMM1 workload, G=32 experts,
+M_max=16, masked_m ~ U{0..8}, N=4096, K=7168).  Each timed step is bracketed by
+CUDA events on the launching stream; L2 is flushed (256 MB write) between
+steps.  Prints one JSON line (rank 0).  Under torchrun every rank runs an
+independent replica (the GEMM has no exchange step): value = all ranks' work /
+the slowest rank's time.
+
+--impl reference times the CPU oracle (the plain C fp64 reference) on the
+host cores instead, each step a bounded random sample of the same workload's
+outputs.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from nvfp4_block_scaled_masked_gb300 import workloads as W  # noqa: E402
+
+METRIC = "grouped NVFP4 GEMM TFLOP/s and weight GB/s, % of roofline, vs oracle"
+UNIT = "TFLOP/s"
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25    # dense nominal ratio (fp4 13.5 PF, bf16 2.25 PF)
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.txt")
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    src="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "nvfp4_block_scaled_masked_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(config_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source for this workload; else None."""
+    try:
+        text = open(PROFILE_TRAFFIC).read()
+    except OSError:
+        return None
+    src = kernel_source_hash()
+    for line in text.splitlines():
+        m = re.match(r"\s*(\w+)\s+source=(\w+)\s+dram_bytes_per_launch=(\d+)", line)
+        if m and m.group(1) == config_key and m.group(2) == src:
+            return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons every 100 ms in a thread."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        self.dev = device_index
+        self.t_on = None
+        self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.dev)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        threading.Thread(target=self._reader, daemon=True).start()
+
+    def _reader(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark_on(self):
+        self.t_on = time.time()
+
+    def mark_off(self):
+        self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "nvidia-smi unavailable"}
+        rows = []
+        for t, line in self.samples:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((t, parts))
+        inside = [r for r in rows if self.t_on and self.t_on - 0.05 <= r[0] <= (self.t_off or 1e30) + 0.05]
+        note = "samples inside the timed region"
+        if not inside:
+            inside = rows[-3:]
+            note = "timed region shorter than the sampling period: nearest samples"
+        mhz = [float(p[1]) for _, p in inside if p[1].replace(".", "").isdigit()]
+        mx = [float(p[2]) for _, p in inside if p[2].replace(".", "").isdigit()]
+        power = [float(p[3]) for _, p in inside if re.match(r"^[\d.]+$", p[3])]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for _, p in inside:
+            for name, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(inside), "note": note}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args, cfg, ws, rank):
+    """The oracle (plain C, fp64, all host cores) on bounded random samples of
+    the workload's valid outputs: one sample per step."""
+    if rank != 0:
+        return
+    from oracle import oracle
+    d = W.generate(cfg)
+    counts = W.algorithmic_counts(cfg, d["masked_m"])
+    mm = d["masked_m"]
+    valid_g = np.flatnonzero(mm > 0)
+    rng = np.random.default_rng(1)
+    cores = oracle.max_threads()
+
+    def sample(n):
+        g = rng.choice(valid_g, n)
+        m = (rng.random(n) * mm[g]).astype(np.int64)
+        nn = rng.integers(0, cfg.N, n)
+        return np.stack([g, m, nn], 1)
+
+    # calibrate: outputs per second, then size each step so that the whole
+    # run stays within ~60 s of CPU time
+    t = time.perf_counter()
+    oracle.gemm_sampled(d["A"], d["A_sf"], d["B"], d["B_sf"], d["alpha"], sample(4096),
+                        cfg.G, cfg.M_max, cfg.N, cfg.K)
+    rate = 4096 / max(time.perf_counter() - t, 1e-6)
+    per_step = int(max(256, min(rate * 60.0 / max(1, args.steps + args.warmup), rate * 2)))
+    for _ in range(args.warmup):
+        oracle.gemm_sampled(d["A"], d["A_sf"], d["B"], d["B_sf"], d["alpha"], sample(per_step),
+                            cfg.G, cfg.M_max, cfg.N, cfg.K)
+    times = []
+    for _ in range(args.steps):
+        idx = sample(per_step)
+        t = time.perf_counter()
+        oracle.gemm_sampled(d["A"], d["A_sf"], d["B"], d["B_sf"], d["alpha"], idx,
+                            cfg.G, cfg.M_max, cfg.N, cfg.K)
+        times.append(time.perf_counter() - t)
+    tot = sum(times)
+    flops = 2.0 * per_step * cfg.K * args.steps
+    value = flops / tot / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_block(cfg, counts),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{per_step} random valid outputs (g,m,n) per step, "
+                                   f"K={cfg.K} fp64 terms each"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_block(cfg, counts):
+    return {"workload": cfg.name, "G": cfg.G, "M_max": cfg.M_max, "N": cfg.N, "K": cfg.K,
+            "masked_rows": counts["rows"], "nonempty_experts": counts["nonempty"],
+            "seed": hex(cfg.seed), "parallelism": "replicas",
+            "l2": "flushed between steps (256 MB write); weights also exceed L2"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="c2", choices=sorted(W.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    cfg = W.CONFIGS[args.config]
+    ws, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        run_reference(args, cfg, ws, rank)
+        return
+
+    import torch
+    from nvfp4_block_scaled_masked_gb300 import binding, build
+    from nvfp4_block_scaled_masked_gb300.device import Problem
+
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    build.build()
+    binding.load()
+    peaks = load_peaks()
+
+    d = W.generate(cfg)
+    counts = W.algorithmic_counts(cfg, d["masked_m"])
+    stream = torch.cuda.current_stream()
+
+    # one-time weight re-layout, timed separately (median of 5)
+    prob = Problem(d, keep_raw_weights=True)
+    prep_ms = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        binding.nvfp4_prepare_weights(prob.raw_B, prob.raw_Bsf, cfg.G, cfg.N, cfg.K, prob.B_prep,
+                                      prob.B_sf_prep)
+        e1.record()
+        e1.synchronize()
+        prep_ms.append(e0.elapsed_time(e1))
+    prob.raw_B = prob.raw_Bsf = None
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for i in range(args.warmup):
+        prob.run()
+    if binding.nvfp4_gg_check_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark_on()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        prob.run()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t_wall
+    sampler.mark_off()
+    sampler.stop()
+    rc = binding.nvfp4_gg_check_error()
+    if rc != 0:
+        raise RuntimeError(f"device error in the timed region: {binding.status_string(rc)}")
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    dev_s = sum(step_ms) / 1e3
+    if ws > 1:
+        t = torch.tensor([dev_s], device="cuda", dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dev_s = float(t.item())
+    ms = 1e3 * dev_s / args.steps
+    tflops = counts["flops"] * ws / (ms / 1e3) / 1e12
+    gbs = counts["bytes"] / (ms / 1e3) / 1e9
+    wgbs = counts["weight_bytes"] / (ms / 1e3) / 1e9
+
+    # end to end through the host-buffer entry point: pinned inputs copied in,
+    # valid rows of C copied out, every step
+    h = {k: torch.from_numpy(np.ascontiguousarray(d[k])).pin_memory()
+         for k in ("A", "A_sf", "alpha", "masked_m")}
+    h["masked_m"] = torch.from_numpy(d["masked_m"].astype(np.int32)).pin_memory()
+    hC = torch.empty((cfg.G, cfg.M_max, cfg.N), dtype=torch.int16).pin_memory()
+    staging_bytes = binding.nvfp4_host_staging_bytes(cfg.G, cfg.M_max, cfg.N, cfg.K)
+    staging = torch.empty(staging_bytes, dtype=torch.uint8, device="cuda")
+
+    def e2e_step():
+        binding.nvfp4_grouped_gemm_nt_masked_host(
+            h["A"], h["A_sf"], h["alpha"], h["masked_m"], prob.B_prep, prob.B_sf_prep, hC,
+            cfg.G, cfg.M_max, cfg.N, cfg.K, staging, staging_bytes)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.e2e_steps):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        stream.synchronize()         # the host reads the result
+        e2e_ms.append(1e3 * (time.perf_counter() - t0))
+    if binding.nvfp4_gg_check_error() != 0:
+        raise RuntimeError("device error in the end-to-end leg")
+    e2e_med = statistics.median(e2e_ms)
+    h2d = sum(h[k].numel() * h[k].element_size() for k in h)
+    d2h = int(d["masked_m"].sum()) * cfg.N * 2
+
+    line = {
+        "metric": METRIC, "value": tflops, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4 (e2m1 x e2m1, e4m3 block-16 scales, f32 accumulate, bf16 out)",
+        "data": "synthetic", "config": config_block(cfg, counts),
+        "algorithmic_gbs": gbs, "weight_gbs": wgbs,
+        "prepare_weights_ms": statistics.median(prep_ms),
+        "gpu_launches": args.steps,
+        "wall_s_timed_region": wall,
+        "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
+    }
+    if cfg.key == "c5":
+        peak = peaks["bf16"] * NOMINAL_FP4_OVER_BF16
+        line["roofline"] = {"bound": "tensor", "achieved": tflops / ws, "peak": peak,
+                            "unit": "TFLOP/s", "frac": tflops / ws / peak,
+                            "traffic": profiled_traffic(cfg.key),
+                            "peak_note": f"nvfp4 = bf16 {peaks['src']} burst x {NOMINAL_FP4_OVER_BF16:g} (nominal ratio)"}
+    else:
+        line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                            "frac": gbs / peaks["hbm"], "traffic": profiled_traffic(cfg.key),
+                            "algorithmic_bytes": counts["bytes"],
+                            "peak_note": f"HBM copy bandwidth, {peaks['src']}"}
+    line["e2e"] = {"value": counts["flops"] / (e2e_med / 1e3) / 1e12, "unit": UNIT,
+                   "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                   "ms_per_step": e2e_med, "steps": args.e2e_steps,
+                   "how": "nvfp4_grouped_gemm_nt_masked_host: pinned host inputs -> device, GEMM, "
+                          "valid rows of C -> pinned host, stream sync; wall clock per step"}
+    line["clocks"] = sampler.summary()
+
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg, d, prob)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(cfg, d, prob):
+    """The oracle as it stands, all host cores, on the full workload when that
+    is small (decode configs) or on a bounded set of experts; the GPU output of
+    the last timed step is checked against it on the same outputs."""
+    from oracle import oracle
+    mm = d["masked_m"]
+    cores = oracle.max_threads()
+    G = cfg.G
+    # choose experts until ~2e10 fp64 multiply-adds (10-30 s of CPU work)
+    budget = 2e10
+    chosen, work = [], 0.0
+    for g in np.flatnonzero(mm > 0):
+        w = float(mm[g]) * cfg.N * cfg.K + cfg.N * cfg.K
+        if chosen and work + w > budget:
+            break
+        chosen.append(int(g))
+        work += w
+    sub_mm = np.zeros_like(mm)
+    sub_mm[chosen] = mm[chosen]
+    t = time.perf_counter()
+    Cref, ref = oracle.gemm(d["A"], d["A_sf"], d["B"], d["B_sf"], d["alpha"], sub_mm, d["C_init"],
+                            G, cfg.M_max, cfg.N, cfg.K)
+    el = time.perf_counter() - t
+    rows = int(sub_mm.sum())
+    flops = 2.0 * rows * cfg.N * cfg.K
+    Cg = prob.C_bits()
+    valid = np.zeros((G, cfg.M_max), bool)
+    for g in chosen:
+        valid[g, :mm[g]] = True
+    vals = (Cg[valid].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    r = ref[valid]
+    ok = oracle.tolerance_ok(vals, r, np.abs(r).max()) if r.size else np.array([True])
+    return {"value": flops / el / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": (f"experts {chosen[0]}..{chosen[-1]} ({len(chosen)} of {int((mm > 0).sum())} "
+                       f"non-empty), all {rows} valid rows x N={cfg.N}, K={cfg.K}, fp64"),
+            "seconds": el,
+            "parity": {"outputs": int(ok.size), "within_tolerance": int(ok.sum())}}
+
+
+if __name__ == "__main__":
+    main()

@@ -63,7 +63,7 @@ typedef enum {
 
 /*
  * Sizes of the prepared weight buffers that nvfp4_prepare_weights writes.
- *   *b_bytes  = G * N * K / 2                        (codes, same layout as B)
+ *   *b_bytes  = G * ceil(N/128) * 128 * K / 2        (codes, tiled)
  *   *sf_bytes = G * ceil(N/128) * (K/64) * 512       (scales in MMA atom order)
  * Returns NVFP4GG_OK or NVFP4GG_ERR_NULL / NVFP4GG_ERR_SHAPE.
  */
@@ -73,13 +73,17 @@ int nvfp4_prepared_weight_bytes(int G, int N, int K, size_t* b_bytes, size_t* sf
  * One-time weight re-layout (run once per weight set, outside the timed GEMM).
  *   B         device u8 [G][N][K/2]   e2m1 codes, K-major
  *   B_sf      device u8 [G][N][K/16]  e4m3 scales, row-major
- *   B_prep    device, b_bytes:  receives the codes (a copy of B; B_prep == B
- *             is allowed and then nothing is copied)
- *   B_sf_prep device, sf_bytes: receives the scales regrouped into 512-byte
- *             atoms, one per (expert, 128-row block of N, 64-element block of
- *             K): byte (i*16 + j*4 + b) of an atom holds the scale of row
- *             128*nb + 32*j + i and K block 4*kc + b (zero past row N).
- * Asynchronous on `stream`.  B_sf_prep must not alias B_sf.
+ *   B_prep    device, b_bytes: the codes as contiguous 16384-byte tiles, one
+ *             per (expert g, 128-row block nb, 256-element K block ks), in
+ *             that order; tile byte r*128 + 16*(c ^ (r % 8)) + i holds byte
+ *             128*ks + 16*c + i of row 128*nb + r (the 128-byte swizzle the
+ *             tensor core reads; zero past row N)
+ *   B_sf_prep device, sf_bytes: the scales regrouped into 512-byte atoms, one
+ *             per (expert, 128-row block of N, 64-element block of K): byte
+ *             (i*16 + j*4 + b) of an atom holds the scale of row
+ *             128*nb + 32*j + i and K block 4*kc + b (zero past row N)
+ * Asynchronous on `stream`.  The outputs must not alias the inputs
+ * (NVFP4GG_ERR_SHAPE otherwise).
  */
 int nvfp4_prepare_weights(const void* B, const void* B_sf, int G, int N, int K,
                           void* B_prep, void* B_sf_prep, void* stream);

@@ -45,9 +45,9 @@ constexpr int kThreads = 192;
 constexpr int kNumBoxes = 5;   // token boxes of 16, 32, 64, 128, 256 rows
 
 struct GemmParams {
-    CUtensorMap tm_w;                // prepared B codes u8 [G][N][K/2], box 128 x 128 rows, SW128
     CUtensorMap tm_a[kNumBoxes];     // A codes u8 [G][M_max][K/2], box 128 x (16 << i), SW128
     CUtensorMap tm_asf[kNumBoxes];   // A_sf u8 [G][M_max][K/16], box 16 x (16 << i)
+    const uint8_t* wq;               // prepared codes: [G][NT][K/256][16384], pre-swizzled tiles
     const uint8_t* wsf;              // prepared scales: [G][NT][K/64][512]
     const float* alpha;
     const int* masked_m;
@@ -75,7 +75,14 @@ struct KCfg {
     static constexpr int SFW_COLS = 16;              // 4 MMAs x 4 columns
     static constexpr int SFT_COLS = 16 * NA;
     static constexpr int SF_COLS = SFW_COLS + SFT_COLS;
-    static constexpr int TMEM_NEED = ACC_BUFS * TT_MAX + STAGES * SF_COLS;
+    // One scale-factor TMEM region per ring stage when TMEM allows; else a
+    // single region rewritten every stage (tcgen05.cp and tcgen05.mma issued
+    // by one thread execute in issue order).
+    static constexpr int SF_BUFS = ACC_BUFS * TT_MAX + STAGES * SF_COLS <= 512 ? STAGES : 1;
+    static constexpr int TMEM_NEED = ACC_BUFS * TT_MAX + SF_BUFS * SF_COLS;
+    // Scale-factor operands of tcgen05.mma are addressed in groups of 4 TMEM
+    // columns: every scale address below is a multiple of 4 columns.
+    static_assert(TT_MAX % 4 == 0 && SF_COLS % 4 == 0 && SFW_COLS % 4 == 0, "SF alignment");
     static_assert(TMEM_NEED <= 512, "TMEM budget");
     static constexpr int TMEM_COLS = pow2_cols(TMEM_NEED);
 
@@ -88,8 +95,8 @@ struct KCfg {
     static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_TAB = (OFF_MISC + 16 + 15) & ~15;
-    // cum[kGroupsMax + 1], gw[kGroupsMax] (w | ntt << 16), gm[kGroupsMax]
-    static constexpr int TAB_BYTES = (3 * kGroupsMax + 1) * 4;
+    // cum[kGroupsMax + 1] (tile prefix), gm[kGroupsMax] (clamped masked_m)
+    static constexpr int TAB_BYTES = (2 * kGroupsMax + 1) * 4;
     static constexpr int SMEM_BYTES = OFF_TAB + TAB_BYTES + 1024;   // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -123,9 +130,17 @@ struct TileCoord {
     int g, nt, t0, w, m;
 };
 
+// Token tiles of an expert with m valid rows: ntt = ceil(m / TT_MAX) tiles of
+// equal width w = ceil(m / ntt) rounded up to 16 (the MMA's N granularity).
+template <int TT_MAX>
+__device__ __forceinline__ int token_tiles(int m) { return (m + TT_MAX - 1) / TT_MAX; }
+__device__ __forceinline__ int token_width(int m, int ntt) {
+    return ntt ? (((m + ntt - 1) / ntt + 15) & ~15) : 0;
+}
+
 // Tile id -> (expert, weight block, first token, token width, masked_m).
-__device__ __forceinline__ TileCoord decode_tile(const int* cum, const int* gw, const int* gm,
-                                                 int G, int tile) {
+template <int TT_MAX>
+__device__ __forceinline__ TileCoord decode_tile(const int* cum, const int* gm, int G, int tile) {
     int lo = 0, hi = G - 1;   // the last g with cum[g] <= tile
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -133,13 +148,12 @@ __device__ __forceinline__ TileCoord decode_tile(const int* cum, const int* gw, 
     }
     TileCoord c;
     c.g = lo;
+    c.m = gm[lo];
     const int local = tile - cum[lo];
-    const int x = gw[lo];
-    c.w = x & 0xFFFF;
-    const int ntt = x >> 16;
+    const int ntt = token_tiles<TT_MAX>(c.m);
+    c.w = token_width(c.m, ntt);
     c.nt = local / ntt;
     c.t0 = (local - c.nt * ntt) * c.w;
-    c.m = gm[lo];
     return c;
 }
 
@@ -162,8 +176,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
     uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int* cum = reinterpret_cast<int*>(sbase + Cfg::OFF_TAB);
-    int* gw = cum + kGroupsMax + 1;
-    int* gm = gw + kGroupsMax;
+    int* gm = cum + kGroupsMax + 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -183,7 +196,6 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         tmem_relinquish();   // this CTA allocates nothing else: let others allocate
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(&p.tm_w);
         for (int i = 0; i < kNumBoxes; ++i) {
             prefetch_tmap(&p.tm_a[i]);
             prefetch_tmap(&p.tm_asf[i]);
@@ -198,9 +210,6 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             record_error(p.err, NVFP4GG_ERR_MASK);
             m = m < 0 ? 0 : p.M_max;
         }
-        const int ntt = (m + TT_MAX - 1) / TT_MAX;
-        const int w = ntt ? (((m + ntt - 1) / ntt + 15) & ~15) : 0;
-        gw[g] = w | (ntt << 16);
         gm[g] = m;
     }
     __syncthreads();
@@ -209,7 +218,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         const int lo = lane * per;
         const int hi = min(p.G, lo + per);
         int sum = 0;
-        for (int g = lo; g < hi; ++g) sum += (gw[g] >> 16) * p.NT;
+        for (int g = lo; g < hi; ++g) sum += token_tiles<TT_MAX>(gm[g]) * p.NT;
         int incl = sum;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -219,7 +228,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         int run = incl - sum;
         for (int g = lo; g < hi; ++g) {
             cum[g] = run;
-            run += (gw[g] >> 16) * p.NT;
+            run += token_tiles<TT_MAX>(gm[g]) * p.NT;
         }
         if (lane == 31) cum[p.G] = incl;
     }
@@ -238,9 +247,10 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             long long issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const TileCoord tc = decode_tile(cum, gw, gm, p.G, tile);
-                const uint8_t* wsf_tile =
-                    p.wsf + ((size_t)tc.g * p.NT + tc.nt) * (size_t)p.KS * Cfg::WSF_STAGE;
+                const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
+                const size_t wtile = ((size_t)tc.g * p.NT + tc.nt) * (size_t)p.KS;
+                const uint8_t* wq_tile = p.wq + wtile * Cfg::W_TILE;
+                const uint8_t* wsf_tile = p.wsf + wtile * Cfg::WSF_STAGE;
                 for (int ks = 0; ks < p.KS; ++ks) {
                     if (!wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort_flag, p.err, p.timeout_ns)) {
                         ok = false;
@@ -248,8 +258,8 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                     }
                     const uint32_t fb = bar_full + 8 * s;
                     mbar_arrive_expect_tx(fb, Cfg::W_TILE + Cfg::WSF_STAGE + tc.w * (128 + 16));
-                    tma_load_3d_hint(base + Cfg::OFF_W + s * Cfg::W_TILE, &p.tm_w, fb, ks * 128,
-                                     tc.nt * 128, tc.g, pol_stream);
+                    bulk_load_hint(base + Cfg::OFF_W + s * Cfg::W_TILE,
+                                   wq_tile + (size_t)ks * Cfg::W_TILE, Cfg::W_TILE, fb, pol_stream);
                     bulk_load_hint(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE,
                                    wsf_tile + (size_t)ks * Cfg::WSF_STAGE, Cfg::WSF_STAGE, fb,
                                    pol_stream);
@@ -287,7 +297,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         uint32_t aph = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-            const TileCoord tc = decode_tile(cum, gw, gm, p.G, tile);
+            const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
             ok = __all_sync(0xffffffffu, wait_bounded(bar_acce + 8 * acc, aph ^ 1u, abort_flag,
                                                       p.err, p.timeout_ns));
             if (!ok) break;
@@ -308,7 +318,8 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                         uint4 v[4] = {};
 #pragma unroll
                         for (int j = 0; j < Cfg::JMAX; ++j)
-                            v[j] = *reinterpret_cast<const uint4*>(plain + (128 * a + 32 * j + lane) * 16);
+                            if (128 * a + 32 * j < TT_MAX)
+                                v[j] = *reinterpret_cast<const uint4*>(plain + (128 * a + 32 * j + lane) * 16);
                         *reinterpret_cast<uint4*>(atoms + (0 * Cfg::NA + a) * 512 + lane * 16) =
                             make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
                         *reinterpret_cast<uint4*>(atoms + (1 * Cfg::NA + a) * 512 + lane * 16) =
@@ -318,12 +329,13 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                         *reinterpret_cast<uint4*>(atoms + (3 * Cfg::NA + a) * 512 + lane * 16) =
                             make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
                     }
+                    fence_proxy_async_smem();
                 }
-                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     tc_fence_after();
-                    const uint32_t sfw = tmem + Cfg::ACC_BUFS * TT_MAX + s * Cfg::SF_COLS;
+                    const uint32_t sfw =
+                        tmem + Cfg::ACC_BUFS * TT_MAX + (Cfg::SF_BUFS == 1 ? 0 : s) * Cfg::SF_COLS;
                     const uint32_t sft = sfw + Cfg::SFW_COLS;
                     const uint32_t wsf_s = base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE;
                     const uint32_t tsfa_s = base + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
@@ -357,7 +369,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-            const TileCoord tc = decode_tile(cum, gw, gm, p.G, tile);
+            const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
             const bool ok = __all_sync(0xffffffffu, wait_bounded(bar_accf + 8 * acc, aph, abort_flag,
                                                                  p.err, p.timeout_ns));
             if (!ok) break;
@@ -438,6 +450,34 @@ __global__ void relayout_weight_scales_kernel(const uint8_t* __restrict__ bsf,
                           : 0u;
         }
         *reinterpret_cast<uint4*>(out + idx * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+    }
+}
+
+// Weight-code re-layout: B u8 [G][N][K/2] -> tiles [G][NT][K/256][128][128]
+// holding rows 128*nt .. +127 and bytes 128*ks .. +127 of each row, stored
+// the way a 128-byte-swizzled TMA load would leave them in shared memory
+// (16-byte chunk c of row r at chunk c ^ (r % 8)), zero for rows >= N.  One
+// thread per 16-byte chunk.
+__global__ void relayout_weight_codes_kernel(const uint8_t* __restrict__ b,
+                                             uint8_t* __restrict__ out, int G, int N, int K) {
+    const int NT = (N + 127) / 128;
+    const int KS = K / 256;
+    const long long chunks = (long long)G * NT * KS * 1024;
+    const size_t row_bytes = (size_t)K / 2;
+    for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < chunks;
+         idx += (long long)gridDim.x * blockDim.x) {
+        const int c = (int)(idx & 7);
+        const int r = (int)((idx >> 3) & 127);
+        long long rest = idx >> 10;
+        const int ks = (int)(rest % KS);
+        rest /= KS;
+        const int nt = (int)(rest % NT);
+        const int g = (int)(rest / NT);
+        const int n = nt * 128 + r;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (n < N)
+            v = *reinterpret_cast<const uint4*>(b + ((size_t)g * N + n) * row_bytes + (size_t)ks * 128 + c * 16);
+        *reinterpret_cast<uint4*>(out + (idx >> 3) * 128 + ((c ^ (r & 7)) * 16)) = v;
     }
 }
 

@@ -111,9 +111,10 @@ int launch_variant(DeviceState* d, int slot, const GemmParams& p, cudaStream_t s
 }
 
 // Decode-sized experts (M_max <= 64): token tiles of at most 32, a deep ring
-// for the weight stream.  Larger experts: token tiles of up to 128.
+// for the weight stream.  Larger experts: token tiles of up to 224, so that a
+// prefill expert's rows usually fit one tile and its weights stream once.
 constexpr int kNarrowTT = 32, kNarrowStages = 8;
-constexpr int kWideTT = 128, kWideStages = 5;
+constexpr int kWideTT = 224, kWideStages = 4;
 
 }  // namespace
 
@@ -138,7 +139,7 @@ int nvfp4_prepared_weight_bytes(int G, int N, int K, size_t* b_bytes, size_t* sf
     if (G < 1 || G > NVFP4GG_MAX_GROUPS || N < NVFP4GG_N_ALIGN || N % NVFP4GG_N_ALIGN ||
         N > (1 << 20) || K < NVFP4GG_K_ALIGN || K % NVFP4GG_K_ALIGN || K > (1 << 20))
         return NVFP4GG_ERR_SHAPE;
-    *b_bytes = (size_t)G * N * (K / 2);
+    *b_bytes = (size_t)G * ((N + 127) / 128) * 128 * (K / 2);
     *sf_bytes = (size_t)G * ((N + 127) / 128) * (K / 64) * 512;
     return NVFP4GG_OK;
 }
@@ -151,19 +152,18 @@ int nvfp4_prepare_weights(const void* B, const void* B_sf, int G, int N, int K, 
     if (rc != NVFP4GG_OK) return rc;
     if (!aligned(B, 16) || !aligned(B_sf, 16) || !aligned(B_prep, 16) || !aligned(B_sf_prep, 16))
         return NVFP4GG_ERR_ALIGN;
-    if (B_sf == B_sf_prep) return NVFP4GG_ERR_SHAPE;
+    if (B == B_prep || B_sf == B_sf_prep) return NVFP4GG_ERR_SHAPE;
     DeviceState* d = nullptr;
     if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (B_prep != B) {
-        if (cudaMemcpyAsync(B_prep, B, bb, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-            return NVFP4GG_ERR_CUDA;
-    }
-    const long long rows = (long long)(sb / 16);
     const int threads = 256;
-    long long blocks = (rows + threads - 1) / threads;
-    if (blocks > 16LL * d->sms) blocks = 16LL * d->sms;
-    relayout_weight_scales_kernel<<<(int)blocks, threads, 0, st>>>(
+    const long long cap = 16LL * d->sms;
+    long long blocks = ((long long)(bb / 16) + threads - 1) / threads;
+    relayout_weight_codes_kernel<<<(int)(blocks < cap ? blocks : cap), threads, 0, st>>>(
+        static_cast<const uint8_t*>(B), static_cast<uint8_t*>(B_prep), G, N, K);
+    if (cudaGetLastError() != cudaSuccess) return NVFP4GG_ERR_CUDA;
+    blocks = ((long long)(sb / 16) + threads - 1) / threads;
+    relayout_weight_scales_kernel<<<(int)(blocks < cap ? blocks : cap), threads, 0, st>>>(
         static_cast<const uint8_t*>(B_sf), static_cast<uint8_t*>(B_sf_prep), G, N, K);
     return cuda_status(cudaGetLastError());
 }
@@ -185,8 +185,6 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
     const uint64_t kb = (uint64_t)K / 2, ks = (uint64_t)K / 16;
-    if ((rc = encode_u8_3d(&p.tm_w, B, kb, N, G, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)) != NVFP4GG_OK)
-        return rc;
     // token boxes of 16 << i rows; boxes that no tile can use repeat the 16-row map
     const int rows_cap = ((M_max + 15) / 16) * 16;
     for (int i = 0; i < kNumBoxes; ++i) {
@@ -199,6 +197,7 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
             NVFP4GG_OK)
             return rc;
     }
+    p.wq = static_cast<const uint8_t*>(B);
     p.wsf = static_cast<const uint8_t*>(B_sf);
     p.alpha = alpha;
     p.masked_m = masked_m;

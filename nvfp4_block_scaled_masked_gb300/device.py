@@ -31,12 +31,15 @@ class Problem:
         b_bytes, sf_bytes = B.nvfp4_prepared_weight_bytes(self.G, self.N, self.K)
         raw_B = to_device(d["B"], device)
         raw_Bsf = to_device(d["B_sf"], device)
-        self.B_prep = raw_B    # codes are used in place (B_prep == B)
+        self.B_prep = torch.empty(b_bytes, dtype=torch.uint8, device=device)
         self.B_sf_prep = torch.empty(sf_bytes, dtype=torch.uint8, device=device)
         B.nvfp4_prepare_weights(raw_B, raw_Bsf, self.G, self.N, self.K, self.B_prep,
                                 self.B_sf_prep, stream)
-        self.raw_Bsf = raw_Bsf if keep_raw_weights else None
-        del raw_Bsf
+        if keep_raw_weights:
+            self.raw_B, self.raw_Bsf = raw_B, raw_Bsf
+        else:
+            self.raw_B = self.raw_Bsf = None
+            del raw_B, raw_Bsf
         self.C = torch.full((self.G, self.M_max, self.N), SENTINEL_BF16, dtype=torch.int16,
                             device=device)
 

@@ -42,6 +42,7 @@ def test_prepared_weight_bytes(lib):
     assert b == 32 * 4096 * 3584
     assert s == 32 * 32 * (7168 // 64) * 512 == 32 * 4096 * 7168 // 16
     b, s = binding.nvfp4_prepared_weight_bytes(2, 144, 512)   # N tail padded to 256 rows
+    assert b == 2 * 256 * 256
     assert s == 2 * 2 * 8 * 512
     for bad in [(0, 128, 256), (1025, 128, 256), (1, 120, 256), (1, 128, 320), (1, 128, 0)]:
         with pytest.raises(binding.NVFP4GGError) as e:
@@ -82,7 +83,8 @@ def test_prepare_weights_argument_checks(lib):
     assert f(None, FAKE, 1, 128, 256, FAKE, FAKE + 4096, None) == binding.ERR_NULL
     assert f(FAKE, FAKE, 1, 100, 256, FAKE, FAKE + 4096, None) == binding.ERR_SHAPE
     assert f(FAKE + 1, FAKE, 1, 128, 256, FAKE, FAKE + 4096, None) == binding.ERR_ALIGN
-    assert f(FAKE, FAKE, 1, 128, 256, FAKE, FAKE, None) == binding.ERR_SHAPE   # scales in place
+    assert f(FAKE, FAKE + 64, 1, 128, 256, FAKE + 128, FAKE + 64, None) == binding.ERR_SHAPE
+    assert f(FAKE, FAKE + 64, 1, 128, 256, FAKE, FAKE + 128, None) == binding.ERR_SHAPE
 
 
 def test_host_variant_argument_checks(lib):

@@ -164,7 +164,8 @@ def test_masked_m_out_of_range_is_flagged(lib):
 
 
 def test_prepare_weights_roundtrip(lib):
-    """Re-layout, then the inverse permutation on the CPU, gives back B_sf."""
+    """Re-layout, then the inverse permutations on the CPU, gives back B and
+    B_sf; rows past N are zero."""
     from nvfp4_block_scaled_masked_gb300 import binding
     G, N, K = 3, 272, 512
     rng = np.random.default_rng(4)
@@ -176,8 +177,13 @@ def test_prepare_weights_roundtrip(lib):
     oS = torch.empty(sb, dtype=torch.uint8, device="cuda")
     binding.nvfp4_prepare_weights(dB, dBsf, G, N, K, oB, oS)
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(oB.cpu().numpy(), b.ravel())
-    NT, KC = (N + 127) // 128, K // 64
+    NT, KC, KS = (N + 127) // 128, K // 64, K // 256
+    tiles = oB.cpu().numpy().reshape(G, NT, KS, 128, 8, 16)     # [g][nt][ks][r][chunk][byte]
+    r = np.arange(128)[:, None]
+    unswz = tiles[:, :, :, r, (np.arange(8)[None, :] ^ (r % 8)), :]   # chunk c read from c ^ r%8
+    back_b = unswz.transpose(0, 1, 3, 2, 4, 5).reshape(G, NT * 128, K // 2)
+    np.testing.assert_array_equal(back_b[:, :N], b)
+    assert np.all(back_b[:, N:] == 0)
     atoms = oS.cpu().numpy().reshape(G, NT, KC, 32, 4, 4)      # [g][nt][kc][i][j][b]
     back = atoms.transpose(0, 1, 4, 3, 2, 5).reshape(G, NT * 128, KC * 4)   # row = 128nt+32j+i
     np.testing.assert_array_equal(back[:, :N], bsf)
