@@ -346,10 +346,13 @@ def main():
     }
     if cfg.key == "c5":
         peak = peaks["bf16"] * NOMINAL_FP4_OVER_BF16
+        probe = {n: mma_peak_tflops(n) for n in (256, 208)}
         line["roofline"] = {"bound": "tensor", "achieved": tflops / ws, "peak": peak,
                             "unit": "TFLOP/s", "frac": tflops / ws / peak,
                             "traffic": profiled_traffic(cfg.key),
-                            "peak_note": f"nvfp4 = bf16 {peaks['src']} burst x {NOMINAL_FP4_OVER_BF16:g} (nominal ratio)"}
+                            "peak_note": f"nvfp4 = bf16 {peaks['src']} burst x {NOMINAL_FP4_OVER_BF16:g} (nominal ratio)",
+                            "mma_probe_tflops": {f"N={n}": v for n, v in probe.items()},
+                            "frac_of_probe_N256": tflops / ws / probe[256]}
     else:
         line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                             "frac": gbs / peaks["hbm"], "traffic": profiled_traffic(cfg.key),
@@ -368,6 +371,27 @@ def main():
         print(json.dumps(line), flush=True)
     if ws > 1:
         dist.destroy_process_group()
+
+
+def mma_peak_tflops(n: int, iters: int = 1 << 16) -> float:
+    """Dense NVFP4 tensor rate from the library's MMA probe: all SMs issue
+    back-to-back M=128, N=n, K=64 block-scaled MMAs; median of 5 launches."""
+    import torch
+    from nvfp4_block_scaled_masked_gb300 import binding
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    binding.nvfp4_gg_mma_peak_probe(iters // 16, n)
+    times = []
+    for _ in range(5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        binding.nvfp4_gg_mma_peak_probe(iters, n)
+        e1.record()
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    if binding.nvfp4_gg_check_error() != 0:
+        raise RuntimeError("device error in the MMA probe")
+    flops = sms * iters * 4 * 2.0 * 128 * n * 64
+    return flops / statistics.median(times) / 1e12
 
 
 def cpu_baseline(cfg, d, prob):

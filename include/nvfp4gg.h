@@ -151,6 +151,15 @@ int nvfp4_gg_check_error(void* stream);
  */
 int nvfp4_gg_selftest_watchdog(long long timeout_ns, void* stream);
 
+/*
+ * Tensor-pipe throughput probe (measurement only; computes nothing useful).
+ * Launches `ctas` CTAs (0 = one per SM), each issuing iters x 4 block-scaled
+ * NVFP4 MMAs of M = 128, N = n (16..256, multiple of 16), K = 64 on resident
+ * shared-memory operands.  FLOPs of one launch: ctas * iters * 4 * 2*128*n*64.
+ * Time it with events on `stream` to get the dense NVFP4 tensor rate.
+ */
+int nvfp4_gg_mma_peak_probe(int iters, int n, int ctas, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* nvfp4_gg_status_string(int status);
 

@@ -34,6 +34,7 @@ EXPORTS = (
     "nvfp4_gg_set_sm_count",
     "nvfp4_gg_check_error",
     "nvfp4_gg_selftest_watchdog",
+    "nvfp4_gg_mma_peak_probe",
     "nvfp4_gg_status_string",
 )
 
@@ -75,6 +76,8 @@ def load():
     lib.nvfp4_gg_check_error.restype = i
     lib.nvfp4_gg_selftest_watchdog.argtypes = [ctypes.c_longlong, vp]
     lib.nvfp4_gg_selftest_watchdog.restype = i
+    lib.nvfp4_gg_mma_peak_probe.argtypes = [i, i, i, vp]
+    lib.nvfp4_gg_mma_peak_probe.restype = i
     lib.nvfp4_gg_status_string.argtypes = [i]
     lib.nvfp4_gg_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -151,6 +154,11 @@ def nvfp4_gg_set_sm_count(sm_count: int):
 def nvfp4_gg_check_error(stream=None) -> int:
     """Synchronises the stream; returns (and clears) the device error word."""
     return int(load().nvfp4_gg_check_error(_stream(stream)))
+
+
+def nvfp4_gg_mma_peak_probe(iters: int, n: int, ctas: int = 0, stream=None):
+    _check(load().nvfp4_gg_mma_peak_probe(iters, n, ctas, _stream(stream)),
+           "nvfp4_gg_mma_peak_probe")
 
 
 def nvfp4_gg_selftest_watchdog(timeout_ns: int, stream=None):

@@ -10,24 +10,30 @@
 // 128-row tensor-core tile even for decode-sized masked_m, and a ragged
 // masked_m wastes at most 15 token columns per tile.
 //
-// Roles (192 threads):
-//   warp 0      TMA producer (one lane): weight tile 128 x 256 codes, its 4
-//               scale atoms (bulk copy), token tile w x 256 codes, and the
-//               token scales (plain rows) into a STAGES-deep shared ring.
-//   warp 1      TMEM owner and MMA issuer: regroups token scales into MMA
-//               atoms (all lanes), copies scale atoms to TMEM (tcgen05.cp),
-//               issues 4 x tcgen05.mma (K = 64 each) per stage from one lane.
-//   warps 2..5  epilogue: tcgen05.ld of the fp32 accumulator (lane = n,
-//               column = token), x alpha[g], bf16 round-to-nearest, stores of
-//               rows m < masked_m[g] only.
+// Roles (224 threads).  A tcgen05 instruction occupies its issuing thread for
+// tens of cycles, so the per-stage tensor-core work is split over two issuing
+// threads:
+//   warp 0      producer (one lane): bulk copy of the 16 KB weight tile and
+//               its 2 KB scale atoms, tiled TMA of w token rows and their
+//               scale rows, into a STAGES-deep shared-memory ring.
+//   warp 1      TMEM owner; MMA thread (one lane): copies the weight-scale
+//               atoms to TMEM, issues 4 x tcgen05.mma (K = 64 each) per stage,
+//               commits the stage back to the producer.
+//   warp 2      scale warp: regroups the token scales of the stage into MMA
+//               atoms (all lanes), copies them to TMEM (one lane) and commits
+//               them to the MMA thread.
+//   warps 3..6  epilogue: tcgen05.ld of the fp32 accumulator (lane = n,
+//               column = token), x alpha[g], bf16 round-to-nearest, a per-warp
+//               shared-memory transpose, 16-byte stores of rows m < masked_m[g].
 // Tiles are walked persistently: CTA b takes tiles b, b + grid, ...; the
 // tile list holds, per expert in order, ceil(N/128) weight blocks times the
 // token tiles of that expert, and experts with masked_m = 0 contribute none.
 //
 // Scale factors in TMEM: the MMA reads the scale of operand row r from TMEM
-// lane r % 32 (any quarter), column base + r / 32, byte = 16-element K block.
-// A 512-byte "atom" of 32 rows x 16 bytes (row i: rows i, i+32, i+64, i+96 x 4
-// K blocks) copied with tcgen05.cp.32x128b.warpx4 lands exactly there.
+// lane r % 32 (any quarter), column base + r / 32, byte = 16-element K block;
+// the base must be a multiple of 4 columns.  A 512-byte "atom" of 32 rows x
+// 16 bytes (row i: rows i, i+32, i+64, i+96 x 4 K blocks) copied with
+// tcgen05.cp.32x128b.warpx4 lands exactly there.
 //
 // Every wait on an mbarrier is bounded (time limit in the parameters); on
 // expiry the waiter records NVFP4GG_ERR_TIMEOUT in the error word, raises a
@@ -41,7 +47,7 @@
 namespace nvfp4gg {
 
 constexpr int kGroupsMax = NVFP4GG_MAX_GROUPS;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kNumBoxes = 5;   // token boxes of 16, 32, 64, 128, 256 rows
 
 struct GemmParams {
@@ -64,6 +70,7 @@ __host__ __device__ constexpr int pow2_cols(int n) {
 template <int TT_MAX, int STAGES>
 struct KCfg {
     static_assert(TT_MAX % 32 == 0 && TT_MAX <= 256, "token tile");
+    static_assert(STAGES >= 3, "ring depth");
     static constexpr int W_TILE = 128 * 128;         // 128 weight rows x 256 codes
     static constexpr int T_TILE = TT_MAX * 128;      // TT_MAX token rows x 256 codes
     static constexpr int WSF_STAGE = 4 * 512;        // 4 weight-scale atoms
@@ -75,10 +82,9 @@ struct KCfg {
     static constexpr int SFW_COLS = 16;              // 4 MMAs x 4 columns
     static constexpr int SFT_COLS = 16 * NA;
     static constexpr int SF_COLS = SFW_COLS + SFT_COLS;
-    // One scale-factor TMEM region per ring stage when TMEM allows; else a
-    // single region rewritten every stage (tcgen05.cp and tcgen05.mma issued
-    // by one thread execute in issue order).
-    static constexpr int SF_BUFS = ACC_BUFS * TT_MAX + STAGES * SF_COLS <= 512 ? STAGES : 1;
+    // One scale-factor TMEM region per ring stage when TMEM allows, else two
+    // regions used alternately (reuse waits for the MMAs that read it).
+    static constexpr int SF_BUFS = ACC_BUFS * TT_MAX + STAGES * SF_COLS <= 512 ? STAGES : 2;
     static constexpr int TMEM_NEED = ACC_BUFS * TT_MAX + SF_BUFS * SF_COLS;
     // Scale-factor operands of tcgen05.mma are addressed in groups of 4 TMEM
     // columns: every scale address below is a multiple of 4 columns.
@@ -91,8 +97,11 @@ struct KCfg {
     static constexpr int OFF_WSF = OFF_T + STAGES * T_TILE;
     static constexpr int OFF_TSFP = OFF_WSF + STAGES * WSF_STAGE;
     static constexpr int OFF_TSFA = OFF_TSFP + STAGES * TSF_PLAIN;
-    static constexpr int OFF_BAR = OFF_TSFA + STAGES * TSF_ATOMS;
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * ACC_BUFS + 1;
+    static constexpr int OFF_EPI = OFF_TSFA + STAGES * TSF_ATOMS;   // 4 warps x 16 tokens x 32 n bf16
+    static constexpr int EPI_BYTES = 4 * 16 * 32 * 2;
+    static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
+    // full, empty, sfready per stage; acc full/empty per buffer; two drains
+    static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_TAB = (OFF_MISC + 16 + 15) & ~15;
     // cum[kGroupsMax + 1] (tile prefix), gm[kGroupsMax] (clamped masked_m)
@@ -170,9 +179,11 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
 
     const uint32_t bar_full = base + Cfg::OFF_BAR;
     const uint32_t bar_empty = bar_full + 8 * STAGES;
-    const uint32_t bar_accf = bar_empty + 8 * STAGES;
+    const uint32_t bar_sfready = bar_empty + 8 * STAGES;
+    const uint32_t bar_accf = bar_sfready + 8 * STAGES;
     const uint32_t bar_acce = bar_accf + 8 * Cfg::ACC_BUFS;
-    const uint32_t bar_done = bar_acce + 8 * Cfg::ACC_BUFS;
+    const uint32_t bar_done = bar_acce + 8 * Cfg::ACC_BUFS;   // MMA thread's drain
+    const uint32_t bar_done2 = bar_done + 8;                  // scale warp's drain
     uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int* cum = reinterpret_cast<int*>(sbase + Cfg::OFF_TAB);
@@ -182,12 +193,14 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
+            mbar_init(bar_sfready + 8 * s, 1);
         }
         for (int b = 0; b < Cfg::ACC_BUFS; ++b) {
             mbar_init(bar_accf + 8 * b, 1);
             mbar_init(bar_acce + 8 * b, 4);
         }
         mbar_init(bar_done, 1);
+        mbar_init(bar_done2, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -202,8 +215,8 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         }
     }
 
-    // Per-expert tables: valid rows, token tiles, token width; then the
-    // exclusive prefix of tile counts (ntt * NT per expert).
+    // Per-expert tables: valid rows (clamped), then the exclusive prefix of
+    // tile counts (token tiles x weight blocks per expert).
     for (int g = threadIdx.x; g < p.G; g += kThreads) {
         int m = __ldg(p.masked_m + g);
         if (m < 0 || m > p.M_max) {
@@ -237,6 +250,9 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const int total = cum[p.G];
+    // TMEM map: accumulators [0, ACC_BUFS*TT_MAX), then SF_BUFS regions of
+    // (16 weight-scale + 16*NA token-scale) columns
+    const uint32_t tmem_sf = tmem + Cfg::ACC_BUFS * TT_MAX;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -290,82 +306,136 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             }
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
+        // ---------------------------------------------------------- MMA thread
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            int acc = 0;
+            uint32_t aph = 0;
+            long long cnt = 0;   // stages consumed so far
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+                const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
+                if (!wait_bounded(bar_acce + 8 * acc, aph ^ 1u, abort_flag, p.err, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t idesc = idesc_mxf4nvf4((uint32_t)tc.w);
+                const uint32_t d_tmem = tmem + acc * TT_MAX;
+                for (int ks = 0; ks < p.KS; ++ks, ++cnt) {
+                    // the stage's operands have landed, and its token scales
+                    // are in TMEM (the scale warp commits after full)
+                    if (!wait_bounded(bar_full + 8 * s, ph, abort_flag, p.err, p.timeout_ns) ||
+                        !wait_bounded(bar_sfready + 8 * s, ph, abort_flag, p.err, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const int rsf = Cfg::SF_BUFS == STAGES ? s : (int)(cnt % Cfg::SF_BUFS);
+                    if (Cfg::SF_BUFS != STAGES && cnt >= Cfg::SF_BUFS) {
+                        // the MMAs that last read this scale region must be done
+                        const long long prev = cnt - Cfg::SF_BUFS;
+                        if (!wait_bounded(bar_empty + 8 * (int)(prev % STAGES),
+                                          (uint32_t)((prev / STAGES) & 1), abort_flag, p.err,
+                                          p.timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    tc_fence_after();
+                    const uint32_t sfw = tmem_sf + rsf * Cfg::SF_COLS;
+                    const uint32_t sft = sfw + Cfg::SFW_COLS;
+                    const uint32_t wsf_s = base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE;
+                    const uint64_t c0 = sdesc_rows16(wsf_s), c1 = sdesc_rows16(wsf_s + 512);
+                    const uint64_t c2 = sdesc_rows16(wsf_s + 1024), c3 = sdesc_rows16(wsf_s + 1536);
+                    const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_W + s * Cfg::W_TILE);
+                    const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_T + s * Cfg::T_TILE);
+                    const uint32_t acc_in = ks != 0;
+                    tmem_cp_32x128b_x4(sfw, c0);
+                    tmem_cp_32x128b_x4(sfw + 4, c1);
+                    tmem_cp_32x128b_x4(sfw + 8, c2);
+                    tmem_cp_32x128b_x4(sfw + 12, c3);
+                    umma_mxf4nvf4(d_tmem, ad, bd, idesc, sfw, sft, acc_in);
+                    umma_mxf4nvf4(d_tmem, ad + 2, bd + 2, idesc, sfw + 4, sft + 4 * Cfg::NA, 1u);
+                    umma_mxf4nvf4(d_tmem, ad + 4, bd + 4, idesc, sfw + 8, sft + 8 * Cfg::NA, 1u);
+                    umma_mxf4nvf4(d_tmem, ad + 6, bd + 6, idesc, sfw + 12, sft + 12 * Cfg::NA, 1u);
+                    umma_commit(bar_empty + 8 * s);
+                    if (ks == p.KS - 1) umma_commit(bar_accf + 8 * acc);
+                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                }
+                if (++acc == Cfg::ACC_BUFS) { acc = 0; aph ^= 1u; }
+            }
+            // Drain the tensor pipe before TMEM is freed.
+            umma_commit(bar_done);
+            volatile int no_abort = 0;
+            wait_bounded(bar_done, 0, &no_abort, p.err, p.timeout_ns);
+        }
+    } else if (warp == 2) {
+        // ------------------------------------------------------- scale warp
         int s = 0;
         uint32_t ph = 0;
-        int acc = 0;
-        uint32_t aph = 0;
+        long long cnt = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-            const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
-            ok = __all_sync(0xffffffffu, wait_bounded(bar_acce + 8 * acc, aph ^ 1u, abort_flag,
-                                                      p.err, p.timeout_ns));
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t idesc = idesc_mxf4nvf4((uint32_t)tc.w);
-            const uint32_t d_tmem = tmem + acc * TT_MAX;
-            for (int ks = 0; ks < p.KS; ++ks) {
+            for (int ks = 0; ks < p.KS; ++ks, ++cnt) {
                 ok = __all_sync(0xffffffffu,
                                 wait_bounded(bar_full + 8 * s, ph, abort_flag, p.err, p.timeout_ns));
                 if (!ok) break;
-                // Token scales: plain rows (token t: 4 words, one per MMA) ->
-                // per-MMA atoms (row i: tokens i, i+32, i+64, i+96).
-                {
-                    const uint8_t* plain = sbase + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN;
-                    uint8_t* atoms = sbase + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
+                // plain rows (token t: 4 words, one per MMA) -> per-MMA atoms
+                // (row i: tokens i, i+32, i+64, i+96)
+                const uint8_t* plain = sbase + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN;
+                uint8_t* atoms = sbase + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
 #pragma unroll
-                    for (int a = 0; a < Cfg::NA; ++a) {
-                        uint4 v[4] = {};
+                for (int a = 0; a < Cfg::NA; ++a) {
+                    uint4 v[4] = {};
 #pragma unroll
-                        for (int j = 0; j < Cfg::JMAX; ++j)
-                            if (128 * a + 32 * j < TT_MAX)
-                                v[j] = *reinterpret_cast<const uint4*>(plain + (128 * a + 32 * j + lane) * 16);
-                        *reinterpret_cast<uint4*>(atoms + (0 * Cfg::NA + a) * 512 + lane * 16) =
-                            make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
-                        *reinterpret_cast<uint4*>(atoms + (1 * Cfg::NA + a) * 512 + lane * 16) =
-                            make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
-                        *reinterpret_cast<uint4*>(atoms + (2 * Cfg::NA + a) * 512 + lane * 16) =
-                            make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
-                        *reinterpret_cast<uint4*>(atoms + (3 * Cfg::NA + a) * 512 + lane * 16) =
-                            make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
-                    }
-                    fence_proxy_async_smem();
+                    for (int j = 0; j < Cfg::JMAX; ++j)
+                        if (128 * a + 32 * j < TT_MAX)
+                            v[j] = *reinterpret_cast<const uint4*>(plain + (128 * a + 32 * j + lane) * 16);
+                    *reinterpret_cast<uint4*>(atoms + (0 * Cfg::NA + a) * 512 + lane * 16) =
+                        make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+                    *reinterpret_cast<uint4*>(atoms + (1 * Cfg::NA + a) * 512 + lane * 16) =
+                        make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
+                    *reinterpret_cast<uint4*>(atoms + (2 * Cfg::NA + a) * 512 + lane * 16) =
+                        make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
+                    *reinterpret_cast<uint4*>(atoms + (3 * Cfg::NA + a) * 512 + lane * 16) =
+                        make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
                 }
+                fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tc_fence_after();
-                    const uint32_t sfw =
-                        tmem + Cfg::ACC_BUFS * TT_MAX + (Cfg::SF_BUFS == 1 ? 0 : s) * Cfg::SF_COLS;
-                    const uint32_t sft = sfw + Cfg::SFW_COLS;
-                    const uint32_t wsf_s = base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE;
-                    const uint32_t tsfa_s = base + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
+                    const int rsf = Cfg::SF_BUFS == STAGES ? s : (int)(cnt % Cfg::SF_BUFS);
+                    if (Cfg::SF_BUFS != STAGES && cnt >= Cfg::SF_BUFS) {
+                        const long long prev = cnt - Cfg::SF_BUFS;
+                        ok = wait_bounded(bar_empty + 8 * (int)(prev % STAGES),
+                                          (uint32_t)((prev / STAGES) & 1), abort_flag, p.err,
+                                          p.timeout_ns);
+                    }
+                    if (ok) {
+                        tc_fence_after();
+                        const uint32_t sft = tmem_sf + rsf * Cfg::SF_COLS + Cfg::SFW_COLS;
+                        const uint32_t tsfa_s = base + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) tmem_cp_32x128b_x4(sfw + 4 * q, sdesc_rows16(wsf_s + 512 * q));
-#pragma unroll
-                    for (int q = 0; q < 4 * Cfg::NA; ++q)
-                        tmem_cp_32x128b_x4(sft + 4 * q, sdesc_rows16(tsfa_s + 512 * q));
-                    const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_W + s * Cfg::W_TILE);
-                    const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_T + s * Cfg::T_TILE);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        umma_mxf4nvf4(d_tmem, ad + 2 * q, bd + 2 * q, idesc, sfw + 4 * q,
-                                      sft + 4 * Cfg::NA * q, (ks | q) != 0);
-                    umma_commit(bar_empty + 8 * s);
-                    if (ks == p.KS - 1) umma_commit(bar_accf + 8 * acc);
+                        for (int q = 0; q < 4 * Cfg::NA; ++q)
+                            tmem_cp_32x128b_x4(sft + 4 * q, sdesc_rows16(tsfa_s + 512 * q));
+                        umma_commit(bar_sfready + 8 * s);
+                    }
                 }
-                __syncwarp();
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
-            if (++acc == Cfg::ACC_BUFS) { acc = 0; aph ^= 1u; }
         }
-        // Drain the tensor pipe before TMEM is freed.
-        if (lane == 0) umma_commit(bar_done);
-        __syncwarp();
-        volatile int no_abort = 0;
-        wait_bounded(bar_done, 0, &no_abort, p.err, p.timeout_ns);
+        // Drain this warp's scale copies before TMEM is freed.
+        if (lane == 0) {
+            umma_commit(bar_done2);
+            volatile int no_abort = 0;
+            wait_bounded(bar_done2, 0, &no_abort, p.err, p.timeout_ns);
+        }
     } else {
         // ------------------------------------------------------------ epilogue
+        const int ew = warp - 3;     // epilogue warp 0..3
         const int quad = warp & 3;   // TMEM lane quarter this warp may access
+        uint8_t* stage_buf = sbase + Cfg::OFF_EPI + ew * (16 * 32 * 2);
         int acc = 0;
         uint32_t aph = 0;
         for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -375,24 +445,34 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             if (!ok) break;
             tc_fence_after();
             const float al = __ldg(p.alpha + tc.g);
-            const int n = tc.nt * 128 + quad * 32 + lane;
+            const int n0 = tc.nt * 128 + quad * 32;   // first of this warp's 32 weight rows
             const int t_end = min(tc.t0 + tc.w, tc.m);
             const uint32_t tbase = tmem + acc * TT_MAX + ((uint32_t)(quad * 32) << 16);
-            __nv_bfloat16* crow = p.C + ((size_t)tc.g * p.M_max) * p.N + n;
+            // each lane later stores 16 bytes: token row (lane >> 2) (+8),
+            // weight rows n0 + 8*(lane & 3) .. +7
+            const int tr = lane >> 2, tq = lane & 3;
+            const bool n_ok = n0 + 8 * tq < p.N;
 #pragma unroll 1
             for (int c = 0; c < TT_MAX / 16; ++c) {
                 if (c * 16 >= tc.w) break;
                 uint32_t r[16];
                 tmem_ld_32x32b_x16(tbase + c * 16, r);
                 tmem_wait_ld();
-                if (n < p.N) {
+                // lane = weight row n0 + lane; column t = token; transpose via
+                // shared memory into [token][32 rows] bf16
+                __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stage_buf);
 #pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const int tok = tc.t0 + c * 16 + t;
-                        if (tok < t_end)
-                            crow[(size_t)tok * p.N] = __float2bfloat16_rn(al * __uint_as_float(r[t]));
-                    }
+                for (int t = 0; t < 16; ++t) sb[t * 32 + lane] = __float2bfloat16_rn(al * __uint_as_float(r[t]));
+                __syncwarp();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = tr + 8 * h;
+                    const int tok = tc.t0 + c * 16 + t;
+                    const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + t * 64 + tq * 16);
+                    if (tok < t_end && n_ok)
+                        *reinterpret_cast<uint4*>(p.C + ((size_t)tc.g * p.M_max + tok) * p.N + n0 + 8 * tq) = v;
                 }
+                __syncwarp();
             }
             tc_fence_before();
             __syncwarp();
@@ -423,6 +503,66 @@ __global__ void watchdog_selftest_kernel(int* err, unsigned long long timeout_ns
     if (threadIdx.x == 0)
         wait_bounded(smem_u32(&bar), 0, &abort_flag, err, timeout_ns);
     __syncthreads();
+}
+
+// Tensor-pipe throughput probe: every CTA issues `iters` x 4 block-scaled
+// MMAs (M = 128, N = n, K = 64 each) on resident shared-memory operands
+// (zero codes, unit scales) into one TMEM accumulator, from one thread, then
+// waits for the tensor pipe with a bounded wait.  FLOPs per CTA:
+// iters * 4 * 2 * 128 * n * 64.
+__global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int n, int* err,
+                                                          unsigned long long timeout_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sbase = smem_raw + (base - raw);
+    // [0, 16K) A tile, [16K, 48K) B tile (256 rows), [48K, 50K) 4 scale
+    // atoms shared by A and B, then the barrier and the TMEM slot
+    constexpr int OFF_SF = 49152, OFF_BAR = 51200, OFF_SLOT = 51208;
+    const int warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < OFF_SF / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(sbase)[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int i = threadIdx.x; i < 2048 / 4; i += blockDim.x)
+        reinterpret_cast<uint32_t*>(sbase + OFF_SF)[i] = 0x38383838u;   // e4m3 1.0
+    if (threadIdx.x == 0) {
+        mbar_init(base + OFF_BAR, 1);
+        fence_mbar_init();
+    }
+    fence_proxy_async_smem();
+    if (warp == 0) {
+        tmem_alloc(base + OFF_SLOT, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + OFF_SLOT);
+    if (threadIdx.x == 0) {
+        const uint32_t sfa = tmem + 256, sfb = tmem + 272;
+        for (int q = 0; q < 4; ++q) {
+            tmem_cp_32x128b_x4(sfa + 4 * q, sdesc_rows16(base + OFF_SF + 512 * q));
+            tmem_cp_32x128b_x4(sfb + 8 * q, sdesc_rows16(base + OFF_SF + 512 * q));
+            tmem_cp_32x128b_x4(sfb + 8 * q + 4, sdesc_rows16(base + OFF_SF + 512 * q));
+        }
+        const uint32_t idesc = idesc_mxf4nvf4((uint32_t)n);
+        const uint64_t ad = sdesc_k_sw128(base);
+        const uint64_t bd = sdesc_k_sw128(base + 16384);
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                umma_mxf4nvf4(tmem, ad + 2 * q, bd + 2 * q, idesc, sfa + 4 * q, sfb + 8 * q,
+                              (it | q) != 0);
+        }
+        umma_commit(base + OFF_BAR);
+        volatile int no_abort = 0;
+        wait_bounded(base + OFF_BAR, 0, &no_abort, err, timeout_ns);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
 }
 
 // Weight-scale re-layout: B_sf u8 [G][N][K/16] -> atoms [G][NT][K/64][32][4][4]

@@ -111,10 +111,10 @@ int launch_variant(DeviceState* d, int slot, const GemmParams& p, cudaStream_t s
 }
 
 // Decode-sized experts (M_max <= 64): token tiles of at most 32, a deep ring
-// for the weight stream.  Larger experts: token tiles of up to 224, so that a
+// for the weight stream.  Larger experts: token tiles of up to 192, so that a
 // prefill expert's rows usually fit one tile and its weights stream once.
 constexpr int kNarrowTT = 32, kNarrowStages = 8;
-constexpr int kWideTT = 224, kWideStages = 4;
+constexpr int kWideTT = 192, kWideStages = 4;
 
 }  // namespace
 
@@ -292,6 +292,22 @@ int nvfp4_gg_selftest_watchdog(long long timeout_ns, void* stream) {
     if (rc != NVFP4GG_OK) return rc;
     watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
         d->err, (unsigned long long)timeout_ns);
+    return cuda_status(cudaGetLastError());
+}
+
+int nvfp4_gg_mma_peak_probe(int iters, int n, int ctas, void* stream) {
+    if (iters < 1 || iters > (1 << 24) || n < 16 || n > 256 || n % 16 != 0 || ctas < 0)
+        return NVFP4GG_ERR_SHAPE;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != NVFP4GG_OK) return rc;
+    constexpr int kSmem = 51216 + 1024;
+    if (cudaFuncSetAttribute(mma_peak_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem) !=
+        cudaSuccess)
+        return NVFP4GG_ERR_CUDA;
+    const int grid = (ctas == 0 || ctas > d->sms) ? d->sms : ctas;
+    mma_peak_kernel<<<grid, 128, kSmem, static_cast<cudaStream_t>(stream)>>>(iters, n, d->err,
+                                                                             g_timeout_ns);
     return cuda_status(cudaGetLastError());
 }
 

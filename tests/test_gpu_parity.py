@@ -152,6 +152,12 @@ def test_watchdog_reports_timeout(lib):
     check_full(d, run_gpu(d))
 
 
+def test_mma_peak_probe_runs_clean(lib):
+    lib.nvfp4_gg_mma_peak_probe(64, 256)
+    lib.nvfp4_gg_mma_peak_probe(64, 16, 3)
+    assert lib.nvfp4_gg_check_error() == 0
+
+
 def test_masked_m_out_of_range_is_flagged(lib):
     from nvfp4_block_scaled_masked_gb300.device import Problem
     d = W.generate(W.custom(2, 16, 128, 256, masked_m=[16, 3]))
