@@ -10,19 +10,19 @@
 // 128-row tensor-core tile even for decode-sized masked_m, and a ragged
 // masked_m wastes at most 15 token columns per tile.
 //
-// Roles (224 threads).  A tcgen05 instruction occupies its issuing thread for
-// tens of cycles, so the per-stage tensor-core work is split over two issuing
-// threads:
-//   warp 0      producer (one lane): bulk copy of the 16 KB weight tile and
-//               its 2 KB scale atoms, tiled TMA of w token rows and their
-//               scale rows, into a STAGES-deep shared-memory ring.
-//   warp 1      TMEM owner; MMA thread (one lane): copies the weight-scale
-//               atoms to TMEM, issues 4 x tcgen05.mma (K = 64 each) per stage,
-//               commits the stage back to the producer.
-//   warp 2      scale warp: regroups the token scales of the stage into MMA
-//               atoms (all lanes), copies them to TMEM (one lane) and commits
-//               them to the MMA thread.
-//   warps 3..6  epilogue: tcgen05.ld of the fp32 accumulator (lane = n,
+// Roles (288 threads).  An asynchronous instruction (TMA copy, mbarrier
+// operation, tcgen05 copy/MMA/commit) occupies its issuing thread for tens of
+// cycles, so the per-stage work is spread over several issuing threads:
+//   warp 0      weight producer (one lane): bulk copies of the 16 KB weight
+//               tile and its 2 KB scale atoms into the shared ring.
+//   warp 1      TMEM owner; MMA thread (one lane): 4 x tcgen05.mma (K = 64
+//               each) per stage, commit of the stage back to the producers.
+//   warp 2      token producer (one lane): one tiled TMA for the w token rows
+//               and one for their scale rows (a tensor map per width w).
+//   warps 3, 4  scale warps (even / odd stages): regroup the token scales
+//               into MMA atoms (all lanes), copy weight and token scale atoms
+//               to TMEM (one lane), commit them to the MMA thread.
+//   warps 5..8  epilogue: tcgen05.ld of the fp32 accumulator (lane = n,
 //               column = token), x alpha[g], bf16 round-to-nearest, a per-warp
 //               shared-memory transpose, 16-byte stores of rows m < masked_m[g].
 // Tiles are walked persistently: CTA b takes tiles b, b + grid, ...; the
@@ -47,12 +47,12 @@
 namespace nvfp4gg {
 
 constexpr int kGroupsMax = NVFP4GG_MAX_GROUPS;
-constexpr int kThreads = 224;
-constexpr int kNumBoxes = 5;   // token boxes of 16, 32, 64, 128, 256 rows
+constexpr int kThreads = 288;
+constexpr int kMaxWidths = 16;   // token tile widths 16, 32, ..., 256 rows
 
 struct GemmParams {
-    CUtensorMap tm_a[kNumBoxes];     // A codes u8 [G][M_max][K/2], box 128 x (16 << i), SW128
-    CUtensorMap tm_asf[kNumBoxes];   // A_sf u8 [G][M_max][K/16], box 16 x (16 << i)
+    CUtensorMap tm_a[kMaxWidths];    // A codes u8 [G][M_max][K/2], box 128 x 16(i+1) rows, SW128
+    CUtensorMap tm_asf[kMaxWidths];  // A_sf u8 [G][M_max][K/16], box 16 x 16(i+1) rows
     const uint8_t* wq;               // prepared codes: [G][NT][K/256][16384], pre-swizzled tiles
     const uint8_t* wsf;              // prepared scales: [G][NT][K/64][512]
     const float* alpha;
@@ -82,10 +82,10 @@ struct KCfg {
     static constexpr int SFW_COLS = 16;              // 4 MMAs x 4 columns
     static constexpr int SFT_COLS = 16 * NA;
     static constexpr int SF_COLS = SFW_COLS + SFT_COLS;
-    // One scale-factor TMEM region per ring stage when TMEM allows, else two
-    // regions used alternately (reuse waits for the MMAs that read it).
-    static constexpr int SF_BUFS = ACC_BUFS * TT_MAX + STAGES * SF_COLS <= 512 ? STAGES : 2;
-    static constexpr int TMEM_NEED = ACC_BUFS * TT_MAX + SF_BUFS * SF_COLS;
+    // One scale-factor TMEM region per ring stage: a region is rewritten only
+    // after the stage's full barrier of the next round, i.e. after the MMAs
+    // that read it completed.
+    static constexpr int TMEM_NEED = ACC_BUFS * TT_MAX + STAGES * SF_COLS;
     // Scale-factor operands of tcgen05.mma are addressed in groups of 4 TMEM
     // columns: every scale address below is a multiple of 4 columns.
     static_assert(TT_MAX % 4 == 0 && SF_COLS % 4 == 0 && SFW_COLS % 4 == 0, "SF alignment");
@@ -100,8 +100,8 @@ struct KCfg {
     static constexpr int OFF_EPI = OFF_TSFA + STAGES * TSF_ATOMS;   // 4 warps x 16 tokens x 32 n bf16
     static constexpr int EPI_BYTES = 4 * 16 * 32 * 2;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    // full, empty, sfready per stage; acc full/empty per buffer; two drains
-    static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 2;
+    // full, empty, sfready per stage; acc full/empty per buffer; three drains
+    static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 3;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_TAB = (OFF_MISC + 16 + 15) & ~15;
     // cum[kGroupsMax + 1] (tile prefix), gm[kGroupsMax] (clamped masked_m)
@@ -177,13 +177,13 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const uint32_t bar_full = base + Cfg::OFF_BAR;
-    const uint32_t bar_empty = bar_full + 8 * STAGES;
-    const uint32_t bar_sfready = bar_empty + 8 * STAGES;
-    const uint32_t bar_accf = bar_sfready + 8 * STAGES;
-    const uint32_t bar_acce = bar_accf + 8 * Cfg::ACC_BUFS;
-    const uint32_t bar_done = bar_acce + 8 * Cfg::ACC_BUFS;   // MMA thread's drain
-    const uint32_t bar_done2 = bar_done + 8;                  // scale warp's drain
+    const uint32_t bar_full = base + Cfg::OFF_BAR;               // 2 producers + bytes
+    const uint32_t bar_empty = bar_full + 8 * STAGES;            // MMA commit
+    const uint32_t bar_sfready = bar_empty + 8 * STAGES;         // scale warp commit
+    const uint32_t bar_accf = bar_sfready + 8 * STAGES;          // MMA commit, last stage
+    const uint32_t bar_acce = bar_accf + 8 * Cfg::ACC_BUFS;      // 4 epilogue warps
+    const uint32_t bar_done = bar_acce + 8 * Cfg::ACC_BUFS;      // MMA thread's drain
+    const uint32_t bar_done2 = bar_done + 8;                     // scale warps' drains (2)
     uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int* cum = reinterpret_cast<int*>(sbase + Cfg::OFF_TAB);
@@ -191,7 +191,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_full + 8 * s, 2);
             mbar_init(bar_empty + 8 * s, 1);
             mbar_init(bar_sfready + 8 * s, 1);
         }
@@ -201,6 +201,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         }
         mbar_init(bar_done, 1);
         mbar_init(bar_done2, 1);
+        mbar_init(bar_done2 + 8, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -208,8 +209,8 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         tmem_alloc(base + Cfg::OFF_MISC, Cfg::TMEM_COLS);
         tmem_relinquish();   // this CTA allocates nothing else: let others allocate
     }
-    if (warp == 0 && lane == 0) {
-        for (int i = 0; i < kNumBoxes; ++i) {
+    if (warp == 2 && lane == 0) {
+        for (int i = 0; i < TT_MAX / 16; ++i) {
             prefetch_tmap(&p.tm_a[i]);
             prefetch_tmap(&p.tm_asf[i]);
         }
@@ -250,60 +251,56 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const int total = cum[p.G];
-    // TMEM map: accumulators [0, ACC_BUFS*TT_MAX), then SF_BUFS regions of
-    // (16 weight-scale + 16*NA token-scale) columns
+    // TMEM map: accumulators [0, ACC_BUFS*TT_MAX), then one region per stage
+    // of 16 weight-scale + 16*NA token-scale columns
     const uint32_t tmem_sf = tmem + Cfg::ACC_BUFS * TT_MAX;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint64_t pol_stream = policy_evict_first();
-            int s = 0;
-            uint32_t ph = 0;
-            long long issued = 0;
-            bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-                const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
-                const size_t wtile = ((size_t)tc.g * p.NT + tc.nt) * (size_t)p.KS;
-                const uint8_t* wq_tile = p.wq + wtile * Cfg::W_TILE;
-                const uint8_t* wsf_tile = p.wsf + wtile * Cfg::WSF_STAGE;
-                for (int ks = 0; ks < p.KS; ++ks) {
-                    if (!wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort_flag, p.err, p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t fb = bar_full + 8 * s;
-                    mbar_arrive_expect_tx(fb, Cfg::W_TILE + Cfg::WSF_STAGE + tc.w * (128 + 16));
+    if ((warp == 0 || warp == 2) && lane == 0) {
+        // ------------------------------------------- producers (weights / tokens)
+        const bool weights = warp == 0;
+        const uint64_t pol_stream = policy_evict_first();
+        int s = 0;
+        uint32_t ph = 0;
+        long long issued = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
+            const size_t wtile = ((size_t)tc.g * p.NT + tc.nt) * (size_t)p.KS;
+            const uint8_t* wq_tile = p.wq + wtile * Cfg::W_TILE;
+            const uint8_t* wsf_tile = p.wsf + wtile * Cfg::WSF_STAGE;
+            const int box = (tc.w >> 4) - 1;   // tensor map of this token width
+            for (int ks = 0; ks < p.KS; ++ks) {
+                if (!wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort_flag, p.err, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = bar_full + 8 * s;
+                if (weights) {
+                    mbar_arrive_expect_tx(fb, Cfg::W_TILE + Cfg::WSF_STAGE);
                     bulk_load_hint(base + Cfg::OFF_W + s * Cfg::W_TILE,
                                    wq_tile + (size_t)ks * Cfg::W_TILE, Cfg::W_TILE, fb, pol_stream);
                     bulk_load_hint(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE,
                                    wsf_tile + (size_t)ks * Cfg::WSF_STAGE, Cfg::WSF_STAGE, fb,
                                    pol_stream);
-                    int r = 0;
-#pragma unroll
-                    for (int i = kNumBoxes - 1; i >= 0; --i) {
-                        if ((16 << i) > TT_MAX) continue;
-                        if ((tc.w >> 4) & (1 << i)) {
-                            tma_load_3d(base + Cfg::OFF_T + s * Cfg::T_TILE + r * 128, &p.tm_a[i], fb,
-                                        ks * 128, tc.t0 + r, tc.g);
-                            tma_load_3d(base + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN + r * 16,
-                                        &p.tm_asf[i], fb, ks * 16, tc.t0 + r, tc.g);
-                            r += 16 << i;
-                        }
-                    }
-                    ++issued;
-                    if (++s == STAGES) { s = 0; ph ^= 1u; }
+                } else {
+                    mbar_arrive_expect_tx(fb, tc.w * (128 + 16));
+                    tma_load_3d(base + Cfg::OFF_T + s * Cfg::T_TILE, &p.tm_a[box], fb, ks * 128,
+                                tc.t0, tc.g);
+                    tma_load_3d(base + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN, &p.tm_asf[box], fb,
+                                ks * 16, tc.t0, tc.g);
                 }
+                ++issued;
+                if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
-            // Drain: every stage's last issued load must have landed before
-            // the CTA may exit (normally already consumed; bounded on abort).
-            for (int st = 0; st < STAGES; ++st) {
-                if (st >= issued) break;
-                const long long last = st + (long long)STAGES * ((issued - 1 - st) / STAGES);
-                const uint32_t par = (uint32_t)((last / STAGES) & 1);
-                volatile int no_abort = 0;
-                wait_bounded(bar_full + 8 * st, par, &no_abort, p.err, p.timeout_ns);
-            }
+        }
+        // Drain: every stage's last issued copy must have landed before the
+        // CTA may exit (normally already consumed; bounded on abort).
+        for (int st = 0; st < STAGES; ++st) {
+            if (st >= issued) break;
+            const long long last = st + (long long)STAGES * ((issued - 1 - st) / STAGES);
+            const uint32_t par = (uint32_t)((last / STAGES) & 1);
+            volatile int no_abort = 0;
+            wait_bounded(bar_full + 8 * st, par, &no_abort, p.err, p.timeout_ns);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA thread
@@ -312,7 +309,6 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             uint32_t ph = 0;
             int acc = 0;
             uint32_t aph = 0;
-            long long cnt = 0;   // stages consumed so far
             bool ok = true;
             for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
                 const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
@@ -320,41 +316,22 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                     ok = false;
                     break;
                 }
-                tc_fence_after();
                 const uint32_t idesc = idesc_mxf4nvf4((uint32_t)tc.w);
                 const uint32_t d_tmem = tmem + acc * TT_MAX;
-                for (int ks = 0; ks < p.KS; ++ks, ++cnt) {
-                    // the stage's operands have landed, and its token scales
-                    // are in TMEM (the scale warp commits after full)
+                for (int ks = 0; ks < p.KS; ++ks) {
+                    // operands landed (full) and both scale sets are in TMEM
+                    // (the scale warp commits only after full)
                     if (!wait_bounded(bar_full + 8 * s, ph, abort_flag, p.err, p.timeout_ns) ||
                         !wait_bounded(bar_sfready + 8 * s, ph, abort_flag, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
-                    const int rsf = Cfg::SF_BUFS == STAGES ? s : (int)(cnt % Cfg::SF_BUFS);
-                    if (Cfg::SF_BUFS != STAGES && cnt >= Cfg::SF_BUFS) {
-                        // the MMAs that last read this scale region must be done
-                        const long long prev = cnt - Cfg::SF_BUFS;
-                        if (!wait_bounded(bar_empty + 8 * (int)(prev % STAGES),
-                                          (uint32_t)((prev / STAGES) & 1), abort_flag, p.err,
-                                          p.timeout_ns)) {
-                            ok = false;
-                            break;
-                        }
-                    }
                     tc_fence_after();
-                    const uint32_t sfw = tmem_sf + rsf * Cfg::SF_COLS;
+                    const uint32_t sfw = tmem_sf + s * Cfg::SF_COLS;
                     const uint32_t sft = sfw + Cfg::SFW_COLS;
-                    const uint32_t wsf_s = base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE;
-                    const uint64_t c0 = sdesc_rows16(wsf_s), c1 = sdesc_rows16(wsf_s + 512);
-                    const uint64_t c2 = sdesc_rows16(wsf_s + 1024), c3 = sdesc_rows16(wsf_s + 1536);
                     const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_W + s * Cfg::W_TILE);
                     const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_T + s * Cfg::T_TILE);
                     const uint32_t acc_in = ks != 0;
-                    tmem_cp_32x128b_x4(sfw, c0);
-                    tmem_cp_32x128b_x4(sfw + 4, c1);
-                    tmem_cp_32x128b_x4(sfw + 8, c2);
-                    tmem_cp_32x128b_x4(sfw + 12, c3);
                     umma_mxf4nvf4(d_tmem, ad, bd, idesc, sfw, sft, acc_in);
                     umma_mxf4nvf4(d_tmem, ad + 2, bd + 2, idesc, sfw + 4, sft + 4 * Cfg::NA, 1u);
                     umma_mxf4nvf4(d_tmem, ad + 4, bd + 4, idesc, sfw + 8, sft + 8 * Cfg::NA, 1u);
@@ -370,70 +347,72 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             volatile int no_abort = 0;
             wait_bounded(bar_done, 0, &no_abort, p.err, p.timeout_ns);
         }
-    } else if (warp == 2) {
-        // ------------------------------------------------------- scale warp
+    } else if (warp == 3 || warp == 4) {
+        // ------------------------------------------ scale warps (even / odd stages)
+        const int parity = warp - 3;
         int s = 0;
         uint32_t ph = 0;
         long long cnt = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
             for (int ks = 0; ks < p.KS; ++ks, ++cnt) {
-                ok = __all_sync(0xffffffffu,
-                                wait_bounded(bar_full + 8 * s, ph, abort_flag, p.err, p.timeout_ns));
-                if (!ok) break;
-                // plain rows (token t: 4 words, one per MMA) -> per-MMA atoms
-                // (row i: tokens i, i+32, i+64, i+96)
-                const uint8_t* plain = sbase + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN;
-                uint8_t* atoms = sbase + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
+                if ((int)(cnt & 1) == parity) {
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar_full + 8 * s, ph, abort_flag,
+                                                              p.err, p.timeout_ns));
+                    if (!ok) break;
+                    // plain rows (token t: 4 words, one per MMA) -> per-MMA
+                    // atoms (row i: tokens i, i+32, i+64, i+96)
+                    const uint8_t* plain = sbase + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN;
+                    uint8_t* atoms = sbase + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
 #pragma unroll
-                for (int a = 0; a < Cfg::NA; ++a) {
-                    uint4 v[4] = {};
+                    for (int a = 0; a < Cfg::NA; ++a) {
+                        uint4 v[4] = {};
 #pragma unroll
-                    for (int j = 0; j < Cfg::JMAX; ++j)
-                        if (128 * a + 32 * j < TT_MAX)
-                            v[j] = *reinterpret_cast<const uint4*>(plain + (128 * a + 32 * j + lane) * 16);
-                    *reinterpret_cast<uint4*>(atoms + (0 * Cfg::NA + a) * 512 + lane * 16) =
-                        make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
-                    *reinterpret_cast<uint4*>(atoms + (1 * Cfg::NA + a) * 512 + lane * 16) =
-                        make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
-                    *reinterpret_cast<uint4*>(atoms + (2 * Cfg::NA + a) * 512 + lane * 16) =
-                        make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
-                    *reinterpret_cast<uint4*>(atoms + (3 * Cfg::NA + a) * 512 + lane * 16) =
-                        make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const int rsf = Cfg::SF_BUFS == STAGES ? s : (int)(cnt % Cfg::SF_BUFS);
-                    if (Cfg::SF_BUFS != STAGES && cnt >= Cfg::SF_BUFS) {
-                        const long long prev = cnt - Cfg::SF_BUFS;
-                        ok = wait_bounded(bar_empty + 8 * (int)(prev % STAGES),
-                                          (uint32_t)((prev / STAGES) & 1), abort_flag, p.err,
-                                          p.timeout_ns);
+                        for (int j = 0; j < Cfg::JMAX; ++j)
+                            if (128 * a + 32 * j < TT_MAX)
+                                v[j] = *reinterpret_cast<const uint4*>(plain + (128 * a + 32 * j + lane) * 16);
+                        *reinterpret_cast<uint4*>(atoms + (0 * Cfg::NA + a) * 512 + lane * 16) =
+                            make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
+                        *reinterpret_cast<uint4*>(atoms + (1 * Cfg::NA + a) * 512 + lane * 16) =
+                            make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
+                        *reinterpret_cast<uint4*>(atoms + (2 * Cfg::NA + a) * 512 + lane * 16) =
+                            make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
+                        *reinterpret_cast<uint4*>(atoms + (3 * Cfg::NA + a) * 512 + lane * 16) =
+                            make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
                     }
-                    if (ok) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
                         tc_fence_after();
-                        const uint32_t sft = tmem_sf + rsf * Cfg::SF_COLS + Cfg::SFW_COLS;
+                        const uint32_t sfw = tmem_sf + s * Cfg::SF_COLS;
+                        const uint32_t sft = sfw + Cfg::SFW_COLS;
+                        const uint32_t wsf_s = base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE;
                         const uint32_t tsfa_s = base + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
+                        const uint64_t c0 = sdesc_rows16(wsf_s), c1 = sdesc_rows16(wsf_s + 512);
+                        const uint64_t c2 = sdesc_rows16(wsf_s + 1024), c3 = sdesc_rows16(wsf_s + 1536);
+                        tmem_cp_32x128b_x4(sfw, c0);
+                        tmem_cp_32x128b_x4(sfw + 4, c1);
+                        tmem_cp_32x128b_x4(sfw + 8, c2);
+                        tmem_cp_32x128b_x4(sfw + 12, c3);
 #pragma unroll
                         for (int q = 0; q < 4 * Cfg::NA; ++q)
                             tmem_cp_32x128b_x4(sft + 4 * q, sdesc_rows16(tsfa_s + 512 * q));
                         umma_commit(bar_sfready + 8 * s);
                     }
+                    __syncwarp();
                 }
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
         }
         // Drain this warp's scale copies before TMEM is freed.
         if (lane == 0) {
-            umma_commit(bar_done2);
+            umma_commit(bar_done2 + 8 * parity);
             volatile int no_abort = 0;
-            wait_bounded(bar_done2, 0, &no_abort, p.err, p.timeout_ns);
+            wait_bounded(bar_done2 + 8 * parity, 0, &no_abort, p.err, p.timeout_ns);
         }
-    } else {
+    } else if (warp >= 5) {
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - 3;     // epilogue warp 0..3
+        const int ew = warp - 5;     // epilogue warp 0..3
         const int quad = warp & 3;   // TMEM lane quarter this warp may access
         uint8_t* stage_buf = sbase + Cfg::OFF_EPI + ew * (16 * 32 * 2);
         int acc = 0;

@@ -86,6 +86,65 @@ int encode_u8_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint
     return r == CUDA_SUCCESS ? NVFP4GG_OK : NVFP4GG_ERR_CUDA;
 }
 
+// Token tensor maps, one per tile width 16, 32, ..., tt_max (widths a call
+// can use: at most M_max rounded up to 16; the others repeat the 16-row map).
+// Encoding costs microseconds per map, so the last few sets are cached by
+// (A, A_sf, G, M_max, K, tt_max).
+struct TokenMaps {
+    const void* A = nullptr;
+    const void* A_sf = nullptr;
+    int G = 0, M_max = 0, K = 0, tt_max = 0, dev = -1;
+    CUtensorMap a[kMaxWidths];
+    CUtensorMap asf[kMaxWidths];
+};
+constexpr int kMapCache = 8;
+TokenMaps g_maps[kMapCache];
+int g_maps_next = 0;
+
+int token_maps(const void* A, const void* A_sf, int G, int M_max, int K, int tt_max,
+               CUtensorMap* out_a, CUtensorMap* out_asf) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4GG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int i = 0; i < kMapCache; ++i) {
+        const TokenMaps& m = g_maps[i];
+        if (m.A == A && m.A_sf == A_sf && m.G == G && m.M_max == M_max && m.K == K &&
+            m.tt_max == tt_max && m.dev == dev) {
+            std::memcpy(out_a, m.a, sizeof(m.a));
+            std::memcpy(out_asf, m.asf, sizeof(m.asf));
+            return NVFP4GG_OK;
+        }
+    }
+    TokenMaps& m = g_maps[g_maps_next];
+    g_maps_next = (g_maps_next + 1) % kMapCache;
+    m.A = nullptr;   // invalid until fully encoded
+    const uint64_t kb = (uint64_t)K / 2, ks = (uint64_t)K / 16;
+    const int rows_cap = ((M_max + 15) / 16) * 16;
+    int rc = NVFP4GG_OK;
+    for (int i = 0; i < kMaxWidths; ++i) {
+        const uint32_t rows = 16u * (i + 1);
+        const uint32_t b = (rows <= (uint32_t)tt_max && rows <= (uint32_t)rows_cap) ? rows : 16u;
+        if (i > 0 && b == 16u) {
+            m.a[i] = m.a[0];
+            m.asf[i] = m.asf[0];
+            continue;
+        }
+        if ((rc = encode_u8_3d(&m.a[i], A, kb, M_max, G, 128, b, CU_TENSOR_MAP_SWIZZLE_128B)) != NVFP4GG_OK ||
+            (rc = encode_u8_3d(&m.asf[i], A_sf, ks, M_max, G, 16, b, CU_TENSOR_MAP_SWIZZLE_NONE)) != NVFP4GG_OK)
+            return rc;
+    }
+    m.A_sf = A_sf;
+    m.G = G;
+    m.M_max = M_max;
+    m.K = K;
+    m.tt_max = tt_max;
+    m.dev = dev;
+    m.A = A;
+    std::memcpy(out_a, m.a, sizeof(m.a));
+    std::memcpy(out_asf, m.asf, sizeof(m.asf));
+    return NVFP4GG_OK;
+}
+
 int check_gemm_shape(int G, int M_max, int N, int K) {
     if (G < 1 || G > NVFP4GG_MAX_GROUPS) return NVFP4GG_ERR_SHAPE;
     if (M_max < 1 || M_max > (1 << 20)) return NVFP4GG_ERR_SHAPE;
@@ -111,10 +170,10 @@ int launch_variant(DeviceState* d, int slot, const GemmParams& p, cudaStream_t s
 }
 
 // Decode-sized experts (M_max <= 64): token tiles of at most 32, a deep ring
-// for the weight stream.  Larger experts: token tiles of up to 192, so that a
+// for the weight stream.  Larger experts: token tiles of up to 160, so that a
 // prefill expert's rows usually fit one tile and its weights stream once.
 constexpr int kNarrowTT = 32, kNarrowStages = 8;
-constexpr int kWideTT = 192, kWideStages = 4;
+constexpr int kWideTT = 160, kWideStages = 4;
 
 }  // namespace
 
@@ -184,19 +243,7 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
     const int tt_max = narrow ? kNarrowTT : kWideTT;
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
-    const uint64_t kb = (uint64_t)K / 2, ks = (uint64_t)K / 16;
-    // token boxes of 16 << i rows; boxes that no tile can use repeat the 16-row map
-    const int rows_cap = ((M_max + 15) / 16) * 16;
-    for (int i = 0; i < kNumBoxes; ++i) {
-        const uint32_t box = 16u << i;
-        const uint32_t b = (box <= (uint32_t)tt_max && box <= (uint32_t)rows_cap) ? box : 16u;
-        if ((rc = encode_u8_3d(&p.tm_a[i], A, kb, M_max, G, 128, b, CU_TENSOR_MAP_SWIZZLE_128B)) !=
-            NVFP4GG_OK)
-            return rc;
-        if ((rc = encode_u8_3d(&p.tm_asf[i], A_sf, ks, M_max, G, 16, b, CU_TENSOR_MAP_SWIZZLE_NONE)) !=
-            NVFP4GG_OK)
-            return rc;
-    }
+    if ((rc = token_maps(A, A_sf, G, M_max, K, tt_max, p.tm_a, p.tm_asf)) != NVFP4GG_OK) return rc;
     p.wq = static_cast<const uint8_t*>(B);
     p.wsf = static_cast<const uint8_t*>(B_sf);
     p.alpha = alpha;
