@@ -100,8 +100,8 @@ struct KCfg {
     static constexpr int OFF_EPI = OFF_TSFA + STAGES * TSF_ATOMS;   // 4 warps x 16 tokens x 32 n bf16
     static constexpr int EPI_BYTES = 4 * 16 * 32 * 2;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    // full, empty, sfready per stage; acc full/empty per buffer; three drains
-    static constexpr int NUM_BARS = 3 * STAGES + 2 * ACC_BUFS + 3;
+    // full, sfull, empty, sfready per stage; acc full/empty per buffer; three drains
+    static constexpr int NUM_BARS = 4 * STAGES + 2 * ACC_BUFS + 3;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_TAB = (OFF_MISC + 16 + 15) & ~15;
     // cum[kGroupsMax + 1] (tile prefix), gm[kGroupsMax] (clamped masked_m)
@@ -177,8 +177,9 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    const uint32_t bar_full = base + Cfg::OFF_BAR;               // 2 producers + bytes
-    const uint32_t bar_empty = bar_full + 8 * STAGES;            // MMA commit
+    const uint32_t bar_full = base + Cfg::OFF_BAR;               // operand tiles: 2 producers + bytes
+    const uint32_t bar_sfull = bar_full + 8 * STAGES;            // scale rows: 2 producers + bytes
+    const uint32_t bar_empty = bar_sfull + 8 * STAGES;           // MMA commit
     const uint32_t bar_sfready = bar_empty + 8 * STAGES;         // scale warp commit
     const uint32_t bar_accf = bar_sfready + 8 * STAGES;          // MMA commit, last stage
     const uint32_t bar_acce = bar_accf + 8 * Cfg::ACC_BUFS;      // 4 epilogue warps
@@ -192,6 +193,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 2);
+            mbar_init(bar_sfull + 8 * s, 2);
             mbar_init(bar_empty + 8 * s, 1);
             mbar_init(bar_sfready + 8 * s, 1);
         }
@@ -274,20 +276,25 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                     ok = false;
                     break;
                 }
+                // scales first (small: the scale warps start on them while the
+                // operand tiles are still in flight), then the operand tile
                 const uint32_t fb = bar_full + 8 * s;
+                const uint32_t sb = bar_sfull + 8 * s;
                 if (weights) {
-                    mbar_arrive_expect_tx(fb, Cfg::W_TILE + Cfg::WSF_STAGE);
+                    mbar_arrive_expect_tx(sb, Cfg::WSF_STAGE);
+                    bulk_load_hint(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE,
+                                   wsf_tile + (size_t)ks * Cfg::WSF_STAGE, Cfg::WSF_STAGE, sb,
+                                   pol_stream);
+                    mbar_arrive_expect_tx(fb, Cfg::W_TILE);
                     bulk_load_hint(base + Cfg::OFF_W + s * Cfg::W_TILE,
                                    wq_tile + (size_t)ks * Cfg::W_TILE, Cfg::W_TILE, fb, pol_stream);
-                    bulk_load_hint(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE,
-                                   wsf_tile + (size_t)ks * Cfg::WSF_STAGE, Cfg::WSF_STAGE, fb,
-                                   pol_stream);
                 } else {
-                    mbar_arrive_expect_tx(fb, tc.w * (128 + 16));
+                    mbar_arrive_expect_tx(sb, tc.w * 16);
+                    tma_load_3d(base + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN, &p.tm_asf[box], sb,
+                                ks * 16, tc.t0, tc.g);
+                    mbar_arrive_expect_tx(fb, tc.w * 128);
                     tma_load_3d(base + Cfg::OFF_T + s * Cfg::T_TILE, &p.tm_a[box], fb, ks * 128,
                                 tc.t0, tc.g);
-                    tma_load_3d(base + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN, &p.tm_asf[box], fb,
-                                ks * 16, tc.t0, tc.g);
                 }
                 ++issued;
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
@@ -301,6 +308,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             const uint32_t par = (uint32_t)((last / STAGES) & 1);
             volatile int no_abort = 0;
             wait_bounded(bar_full + 8 * st, par, &no_abort, p.err, p.timeout_ns);
+            wait_bounded(bar_sfull + 8 * st, par, &no_abort, p.err, p.timeout_ns);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA thread
@@ -319,8 +327,8 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                 const uint32_t idesc = idesc_mxf4nvf4((uint32_t)tc.w);
                 const uint32_t d_tmem = tmem + acc * TT_MAX;
                 for (int ks = 0; ks < p.KS; ++ks) {
-                    // operands landed (full) and both scale sets are in TMEM
-                    // (the scale warp commits only after full)
+                    // operand tiles landed (full) and both scale sets are in
+                    // TMEM (the scale warp commits after its copies)
                     if (!wait_bounded(bar_full + 8 * s, ph, abort_flag, p.err, p.timeout_ns) ||
                         !wait_bounded(bar_sfready + 8 * s, ph, abort_flag, p.err, p.timeout_ns)) {
                         ok = false;
@@ -357,7 +365,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
             for (int ks = 0; ks < p.KS; ++ks, ++cnt) {
                 if ((int)(cnt & 1) == parity) {
-                    ok = __all_sync(0xffffffffu, wait_bounded(bar_full + 8 * s, ph, abort_flag,
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar_sfull + 8 * s, ph, abort_flag,
                                                               p.err, p.timeout_ns));
                     if (!ok) break;
                     // plain rows (token t: 4 words, one per MMA) -> per-MMA
