@@ -5,8 +5,9 @@ python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl ours|r
 One step = one call of nvfp4_grouped_gemm_nt_masked over one batch of the
 synthetic workload (default: the decode GEMM1 workload, G=32 experts,
 M_max=16, masked_m ~ U{0..8}, N=4096, K=7168).  Each timed step is bracketed by
-CUDA events on the launching stream; L2 is flushed (256 MB write) between
-steps.  Prints one JSON line (rank 0).  Under torchrun every rank runs an
+CUDA events on the launching stream; between steps L2 is flushed by writing a
+256 MB buffer and then reading it back, so the next step starts with an L2
+that holds none of its inputs and no dirty lines.  Prints one JSON line (rank 0).  Under torchrun every rank runs an
 independent replica (the GEMM has no exchange step): value = all ranks' work /
 the slowest rank's time.
 
@@ -211,7 +212,27 @@ def config_block(cfg, counts):
     return {"workload": cfg.name, "G": cfg.G, "M_max": cfg.M_max, "N": cfg.N, "K": cfg.K,
             "masked_rows": counts["rows"], "nonempty_experts": counts["nonempty"],
             "seed": hex(cfg.seed), "parallelism": "replicas",
-            "l2": "flushed between steps (256 MB write); weights also exceed L2"}
+            "l2": "flushed between steps: 256 MB written, then read back (clean L2)"}
+
+
+def replica_seconds(local_seconds: float, world_size: int) -> float:
+    """Max over ranks of the device time of the timed steps (the slowest
+    replica sets the job's time); identity on one rank."""
+    if world_size <= 1:
+        return local_seconds
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_seconds], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def flush_l2(buf, i):
+    """Evict L2: write a buffer larger than L2, then read it back so the
+    evicted lines are clean when the timed step starts."""
+    buf.fill_(i & 0xFF)
+    return buf.sum()
 
 
 def main():
@@ -278,7 +299,7 @@ def main():
     sampler.mark_on()
     t_wall = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush, i)
         starts[i].record(stream)
         prob.run()
         ends[i].record(stream)
@@ -292,11 +313,7 @@ def main():
     if rc != 0:
         raise RuntimeError(f"device error in the timed region: {binding.status_string(rc)}")
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    dev_s = sum(step_ms) / 1e3
-    if ws > 1:
-        t = torch.tensor([dev_s], device="cuda", dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dev_s = float(t.item())
+    dev_s = replica_seconds(sum(step_ms) / 1e3, ws)
     ms = 1e3 * dev_s / args.steps
     tflops = counts["flops"] * ws / (ms / 1e3) / 1e12
     gbs = counts["bytes"] / (ms / 1e3) / 1e9
@@ -321,7 +338,7 @@ def main():
     torch.cuda.synchronize()
     e2e_ms = []
     for i in range(args.e2e_steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(flush, i)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
         e2e_step()

@@ -152,6 +152,48 @@ def test_watchdog_reports_timeout(lib):
     check_full(d, run_gpu(d))
 
 
+def test_host_buffer_entry_point_matches_device_path(lib):
+    """nvfp4_grouped_gemm_nt_masked_host: pinned host inputs in, valid rows of
+    C out; bit-identical to the device-buffer call, other host rows untouched."""
+    from nvfp4_block_scaled_masked_gb300.device import Problem
+    cfg = W.custom(5, 40, 272, 512, masked_m=[40, 0, 17, 33, 1])
+    d = W.generate(cfg, seed=77)
+    prob = Problem(d)
+    prob.run()
+    want = prob.C_bits()
+    h = {k: torch.from_numpy(np.ascontiguousarray(d[k])).pin_memory() for k in ("A", "A_sf", "alpha")}
+    h["masked_m"] = torch.from_numpy(d["masked_m"].astype(np.int32)).pin_memory()
+    hC = torch.full((cfg.G, cfg.M_max, cfg.N), W.SENTINEL_BF16, dtype=torch.int16).pin_memory()
+    nbytes = lib.nvfp4_host_staging_bytes(cfg.G, cfg.M_max, cfg.N, cfg.K)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    for _ in range(2):
+        lib.nvfp4_grouped_gemm_nt_masked_host(h["A"], h["A_sf"], h["alpha"], h["masked_m"],
+                                              prob.B_prep, prob.B_sf_prep, hC, cfg.G, cfg.M_max,
+                                              cfg.N, cfg.K, staging, nbytes)
+        torch.cuda.synchronize()
+        assert lib.nvfp4_gg_check_error() == 0
+        np.testing.assert_array_equal(hC.numpy().view(np.uint16), want)
+    check_full(d, hC.numpy().view(np.uint16))
+
+
+def test_sm_count_cap_gives_identical_results(lib):
+    from nvfp4_block_scaled_masked_gb300.device import Problem
+    d = W.generate(W.custom(3, 200, 384, 512, masked_m=[200, 5, 130]), seed=8)
+    prob = Problem(d)
+    prob.run()
+    ref = prob.C_bits()
+    try:
+        for cap in (1, 7):
+            lib.nvfp4_gg_set_sm_count(cap)
+            prob.reset_C()
+            prob.run()
+            assert lib.nvfp4_gg_check_error() == 0
+            np.testing.assert_array_equal(prob.C_bits(), ref)
+    finally:
+        lib.nvfp4_gg_set_sm_count(0)
+    check_full(d, ref)
+
+
 def test_mma_peak_probe_runs_clean(lib):
     lib.nvfp4_gg_mma_peak_probe(64, 256)
     lib.nvfp4_gg_mma_peak_probe(64, 16, 3)
