@@ -32,6 +32,7 @@ EXPORTS = (
     "nvfp4_host_staging_bytes",
     "nvfp4_grouped_gemm_nt_masked_host",
     "nvfp4_gg_set_sm_count",
+    "nvfp4_gg_set_pair_mode",
     "nvfp4_gg_check_error",
     "nvfp4_gg_selftest_watchdog",
     "nvfp4_gg_mma_peak_probe",
@@ -72,6 +73,8 @@ def load():
     lib.nvfp4_grouped_gemm_nt_masked_host.restype = i
     lib.nvfp4_gg_set_sm_count.argtypes = [i]
     lib.nvfp4_gg_set_sm_count.restype = i
+    lib.nvfp4_gg_set_pair_mode.argtypes = [i]
+    lib.nvfp4_gg_set_pair_mode.restype = i
     lib.nvfp4_gg_check_error.argtypes = [vp]
     lib.nvfp4_gg_check_error.restype = i
     lib.nvfp4_gg_selftest_watchdog.argtypes = [ctypes.c_longlong, vp]
@@ -149,6 +152,10 @@ def nvfp4_grouped_gemm_nt_masked_host(h_A, h_A_sf, h_alpha, h_masked_m, B, B_sf,
 
 def nvfp4_gg_set_sm_count(sm_count: int):
     _check(load().nvfp4_gg_set_sm_count(sm_count), "nvfp4_gg_set_sm_count")
+
+
+def nvfp4_gg_set_pair_mode(enable: bool):
+    _check(load().nvfp4_gg_set_pair_mode(1 if enable else 0), "nvfp4_gg_set_pair_mode")
 
 
 def nvfp4_gg_check_error(stream=None) -> int:

@@ -9,6 +9,7 @@
 #include <mutex>
 
 #include "gemm.cuh"
+#include "gemm_pair.cuh"
 #include "nvfp4gg.h"
 
 using namespace nvfp4gg;
@@ -31,6 +32,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 int g_sm_cap = 0;
+bool g_pair_enabled = false;   // CTA-pair prefill kernel: opt-in (see nvfp4gg.h)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 unsigned long long g_timeout_ns = 2000000000ull;   // 2 s per device-side wait
 
@@ -169,11 +171,43 @@ int launch_variant(DeviceState* d, int slot, const GemmParams& p, cudaStream_t s
     return cuda_status(cudaGetLastError());
 }
 
+template <int TT, int ST>
+int launch_pair_variant(DeviceState* d, int slot, const GemmParams& p, cudaStream_t stream) {
+    using Cfg = PairCfg<TT, ST>;
+    auto kern = gemm_nt_masked_pair_kernel<TT, ST>;
+    if (!d->attr_set[slot]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM_BYTES) != cudaSuccess)
+            return NVFP4GG_ERR_CUDA;
+        d->attr_set[slot] = true;
+    }
+    int ctas = d->sms;
+    if (g_sm_cap > 0 && g_sm_cap < ctas) ctas = g_sm_cap;
+    ctas &= ~1;
+    if (ctas < 2) ctas = 2;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas, 1, 1);
+    cfg.blockDim = dim3(kPairThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, p));
+}
+
 // Decode-sized experts (M_max <= 64): token tiles of at most 32, a deep ring
 // for the weight stream.  Larger experts: token tiles of up to 160, so that a
 // prefill expert's rows usually fit one tile and its weights stream once.
 constexpr int kNarrowTT = 32, kNarrowStages = 8;
 constexpr int kWideTT = 160, kWideStages = 4;
+// Larger experts with N a multiple of 256: CTA pairs (M = 256 per MMA),
+// token tiles of up to 160 split 80 + 80 rows, six ring stages.
+constexpr int kPairTT = 160, kPairStages = 6;
 
 }  // namespace
 
@@ -240,7 +274,8 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
     if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
 
     const bool narrow = M_max <= 64;
-    const int tt_max = narrow ? kNarrowTT : kWideTT;
+    const bool pair = !narrow && N % 256 == 0 && g_pair_enabled;
+    const int tt_max = narrow ? kNarrowTT : pair ? kPairTT : kWideTT;
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
     if ((rc = token_maps(A, A_sf, G, M_max, K, tt_max, p.tm_a, p.tm_asf)) != NVFP4GG_OK) return rc;
@@ -259,6 +294,7 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
     p.timeout_ns = g_timeout_ns;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (narrow) return launch_variant<kNarrowTT, kNarrowStages>(d, 0, p, st);
+    if (pair) return launch_pair_variant<kPairTT, kPairStages>(d, 2, p, st);
     return launch_variant<kWideTT, kWideStages>(d, 1, p, st);
 }
 
@@ -312,6 +348,13 @@ int nvfp4_gg_set_sm_count(int sm_count) {
     if (sm_count < 0) return NVFP4GG_ERR_SHAPE;
     std::lock_guard<std::mutex> lock(g_mu);
     g_sm_cap = sm_count;
+    return NVFP4GG_OK;
+}
+
+int nvfp4_gg_set_pair_mode(int enable) {
+    if (enable != 0 && enable != 1) return NVFP4GG_ERR_SHAPE;
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_pair_enabled = enable != 0;
     return NVFP4GG_OK;
 }
 

@@ -122,6 +122,31 @@ def test_shapes_ragged_and_edges(lib, G, M_max, N, K, masked):
     check_full(d, run_gpu(d))
 
 
+@pytest.mark.parametrize("G,M_max,N,K,masked", [
+    (3, 200, 512, 512, [200, 33, 1]),          # CTA pairs: 2 token tiles, widths 128 / 64 / 32
+    (2, 161, 256, 256, [161, 160]),             # widths rounded to 32, one k-stage
+    (4, 96, 768, 1024, [96, 0, 65, 31]),        # empty expert, 3 weight-block pairs, 4 k-stages
+])
+@pytest.mark.parametrize("pair", [True, False])
+def test_prefill_variants_pair_and_single(lib, G, M_max, N, K, masked, pair):
+    d = W.generate(W.custom(G, M_max, N, K, masked_m=masked), seed=G + N + K)
+    lib.nvfp4_gg_set_pair_mode(pair)
+    try:
+        check_full(d, run_gpu(d))
+    finally:
+        lib.nvfp4_gg_set_pair_mode(False)
+
+
+@pytest.mark.parametrize("key", ["c4", "c5"])
+def test_full_size_sampled_pair_kernel(lib, key):
+    lib.nvfp4_gg_set_pair_mode(True)
+    try:
+        d = W.generate(W.CONFIGS[key])
+        check_sampled(d, run_gpu(d), rows_per_group=3, cols=48)
+    finally:
+        lib.nvfp4_gg_set_pair_mode(False)
+
+
 def test_c2_decode_full(lib):
     d = W.generate(W.CONFIGS["c2"])
     check_full(d, run_gpu(d))
