@@ -228,11 +228,16 @@ def replica_seconds(local_seconds: float, world_size: int) -> float:
     return float(t.item())
 
 
+def torch_int64():
+    import torch
+    return torch.int64
+
+
 def flush_l2(buf, i):
     """Evict L2: write a buffer larger than L2, then read it back so the
     evicted lines are clean when the timed step starts."""
     buf.fill_(i & 0xFF)
-    return buf.sum()
+    return buf.view(torch_int64()).sum()
 
 
 def main():
