@@ -110,6 +110,29 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
                                  void* C, int G, int M_max, int N, int K, void* stream);
 
 /*
+ * Split-K variant for decode-sized calls (M_max <= 64), the swap-AB path's
+ * split-K: each weight tile's K range is cut into split_k contiguous ranges
+ * computed by different CTAs, each leaving an fp32 partial in `workspace`;
+ * the last range of a tile to finish sums the partials in range order (so
+ * results are deterministic), applies alpha and stores bf16.  This keeps all
+ * SMs streaming weights when there are fewer weight tiles than SMs (few
+ * non-empty experts, small N).
+ *   split_k    1..16, or 0 to choose from the tile count: floor(SMs / tiles),
+ *              at most K/256 and 16
+ *   workspace  device scratch owned by the caller, 256-byte aligned, at least
+ *              nvfp4_splitk_workspace_bytes(G, M_max, N, K, split_k) bytes;
+ *              calls that run at the same time must not share it
+ * Other arguments as in nvfp4_grouped_gemm_nt_masked.  With M_max > 64 the
+ * call runs unsplit and the workspace is not touched.  Results agree with the
+ * unsplit call up to fp32 summation order.
+ */
+size_t nvfp4_splitk_workspace_bytes(int G, int M_max, int N, int K, int split_k);
+int nvfp4_grouped_gemm_nt_masked_splitk(const void* A, const void* A_sf, const void* B,
+                                        const void* B_sf, const float* alpha, const int* masked_m,
+                                        void* C, int G, int M_max, int N, int K, int split_k,
+                                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * End-to-end variant for callers whose activations live in host memory.
  *   h_A, h_A_sf, h_alpha, h_masked_m: HOST buffers laid out as above (pinned
  *       memory gives asynchronous copies)

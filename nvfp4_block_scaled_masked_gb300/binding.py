@@ -29,6 +29,8 @@ EXPORTS = (
     "nvfp4_prepared_weight_bytes",
     "nvfp4_prepare_weights",
     "nvfp4_grouped_gemm_nt_masked",
+    "nvfp4_splitk_workspace_bytes",
+    "nvfp4_grouped_gemm_nt_masked_splitk",
     "nvfp4_host_staging_bytes",
     "nvfp4_grouped_gemm_nt_masked_host",
     "nvfp4_gg_set_sm_count",
@@ -67,6 +69,10 @@ def load():
     lib.nvfp4_prepare_weights.restype = i
     lib.nvfp4_grouped_gemm_nt_masked.argtypes = [vp] * 7 + [i] * 4 + [vp]
     lib.nvfp4_grouped_gemm_nt_masked.restype = i
+    lib.nvfp4_splitk_workspace_bytes.argtypes = [i] * 5
+    lib.nvfp4_splitk_workspace_bytes.restype = sz
+    lib.nvfp4_grouped_gemm_nt_masked_splitk.argtypes = [vp] * 7 + [i] * 5 + [vp, sz, vp]
+    lib.nvfp4_grouped_gemm_nt_masked_splitk.restype = i
     lib.nvfp4_host_staging_bytes.argtypes = [i] * 4
     lib.nvfp4_host_staging_bytes.restype = sz
     lib.nvfp4_grouped_gemm_nt_masked_host.argtypes = [vp] * 7 + [i] * 4 + [vp, sz, vp]
@@ -136,6 +142,18 @@ def nvfp4_grouped_gemm_nt_masked(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max,
                                                _ptr(alpha), _ptr(masked_m), _ptr(C),
                                                G, M_max, N, K, _stream(stream)),
            "nvfp4_grouped_gemm_nt_masked")
+
+
+def nvfp4_splitk_workspace_bytes(G, M_max, N, K, split_k=0) -> int:
+    return int(load().nvfp4_splitk_workspace_bytes(G, M_max, N, K, split_k))
+
+
+def nvfp4_grouped_gemm_nt_masked_splitk(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K,
+                                        split_k, workspace, workspace_bytes, stream=None):
+    _check(load().nvfp4_grouped_gemm_nt_masked_splitk(
+        _ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf), _ptr(alpha), _ptr(masked_m), _ptr(C),
+        G, M_max, N, K, split_k, _ptr(workspace), workspace_bytes, _stream(stream)),
+        "nvfp4_grouped_gemm_nt_masked_splitk")
 
 
 def nvfp4_host_staging_bytes(G, M_max, N, K) -> int:

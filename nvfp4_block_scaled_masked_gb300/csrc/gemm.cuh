@@ -61,7 +61,20 @@ struct GemmParams {
     int* err;
     int G, M_max, N, K, NT, KS;
     unsigned long long timeout_ns;
+    // split-K (decode kernel): each tile's K stages are cut into `split`
+    // contiguous ranges computed by different CTAs; with split > 1 every range
+    // leaves an fp32 partial in ws_part[(tile*split + range)][TT_MAX][128] and
+    // the last range to finish (counter ws_cnt[tile]) sums them in range order
+    int split;
+    float* ws_part;
+    int* ws_cnt;
 };
+
+// K stages [kb, ke) of split range sp of S over KS stages (balanced).
+__device__ __forceinline__ void k_range(int sp, int S, int KS, int& kb, int& ke) {
+    kb = (int)(((long long)sp * KS) / S);
+    ke = (int)(((long long)(sp + 1) * KS) / S);
+}
 
 __host__ __device__ constexpr int pow2_cols(int n) {
     return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
@@ -109,6 +122,11 @@ struct KCfg {
     static constexpr int SMEM_BYTES = OFF_TAB + TAB_BYTES + 1024;   // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
+
+// Barrier among `threads` threads (whole warps) on hardware barrier `id`.
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
 
 __device__ __forceinline__ void record_error(int* err, int code) {
     atomicCAS(err, 0, code);
@@ -187,6 +205,8 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
     const uint32_t bar_done2 = bar_done + 8;                     // scale warps' drains (2)
     uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+    volatile int* epi_flag = reinterpret_cast<volatile int*>(misc + 2);   // split-K: last range
+    volatile int* epi_stop = reinterpret_cast<volatile int*>(misc + 3);   // split-K: leave the loop
     int* cum = reinterpret_cast<int*>(sbase + Cfg::OFF_TAB);
     int* gm = cum + kGroupsMax + 1;
 
@@ -253,6 +273,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
     tc_fence_after();
     const uint32_t tmem = misc[0];
     const int total = cum[p.G];
+    const int units = total * p.split;   // (tile, K range) work units
     // TMEM map: accumulators [0, ACC_BUFS*TT_MAX), then one region per stage
     // of 16 weight-scale + 16*NA token-scale columns
     const uint32_t tmem_sf = tmem + Cfg::ACC_BUFS * TT_MAX;
@@ -265,13 +286,16 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         uint32_t ph = 0;
         long long issued = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const int tile = u / p.split;
+            int kb, ke;
+            k_range(u - tile * p.split, p.split, p.KS, kb, ke);
             const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
             const size_t wtile = ((size_t)tc.g * p.NT + tc.nt) * (size_t)p.KS;
             const uint8_t* wq_tile = p.wq + wtile * Cfg::W_TILE;
             const uint8_t* wsf_tile = p.wsf + wtile * Cfg::WSF_STAGE;
             const int box = (tc.w >> 4) - 1;   // tensor map of this token width
-            for (int ks = 0; ks < p.KS; ++ks) {
+            for (int ks = kb; ks < ke; ++ks) {
                 if (!wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort_flag, p.err, p.timeout_ns)) {
                     ok = false;
                     break;
@@ -318,7 +342,10 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             int acc = 0;
             uint32_t aph = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+                const int tile = u / p.split;
+                int kb, ke;
+                k_range(u - tile * p.split, p.split, p.KS, kb, ke);
                 const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
                 if (!wait_bounded(bar_acce + 8 * acc, aph ^ 1u, abort_flag, p.err, p.timeout_ns)) {
                     ok = false;
@@ -326,7 +353,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                 }
                 const uint32_t idesc = idesc_mxf4nvf4((uint32_t)tc.w);
                 const uint32_t d_tmem = tmem + acc * TT_MAX;
-                for (int ks = 0; ks < p.KS; ++ks) {
+                for (int ks = kb; ks < ke; ++ks) {
                     // operand tiles landed (full) and both scale sets are in
                     // TMEM (the scale warp commits after its copies)
                     if (!wait_bounded(bar_full + 8 * s, ph, abort_flag, p.err, p.timeout_ns) ||
@@ -339,13 +366,13 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                     const uint32_t sft = sfw + Cfg::SFW_COLS;
                     const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_W + s * Cfg::W_TILE);
                     const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_T + s * Cfg::T_TILE);
-                    const uint32_t acc_in = ks != 0;
+                    const uint32_t acc_in = ks != kb;
                     umma_mxf4nvf4(d_tmem, ad, bd, idesc, sfw, sft, acc_in);
                     umma_mxf4nvf4(d_tmem, ad + 2, bd + 2, idesc, sfw + 4, sft + 4 * Cfg::NA, 1u);
                     umma_mxf4nvf4(d_tmem, ad + 4, bd + 4, idesc, sfw + 8, sft + 8 * Cfg::NA, 1u);
                     umma_mxf4nvf4(d_tmem, ad + 6, bd + 6, idesc, sfw + 12, sft + 12 * Cfg::NA, 1u);
                     umma_commit(bar_empty + 8 * s);
-                    if (ks == p.KS - 1) umma_commit(bar_accf + 8 * acc);
+                    if (ks == ke - 1) umma_commit(bar_accf + 8 * acc);
                     if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
                 if (++acc == Cfg::ACC_BUFS) { acc = 0; aph ^= 1u; }
@@ -362,8 +389,11 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         uint32_t ph = 0;
         long long cnt = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-            for (int ks = 0; ks < p.KS; ++ks, ++cnt) {
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const int tile = u / p.split;
+            int kb, ke;
+            k_range(u - tile * p.split, p.split, p.KS, kb, ke);
+            for (int ks = kb; ks < ke; ++ks, ++cnt) {
                 if ((int)(cnt & 1) == parity) {
                     ok = __all_sync(0xffffffffu, wait_bounded(bar_sfull + 8 * s, ph, abort_flag,
                                                               p.err, p.timeout_ns));
@@ -425,11 +455,13 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         uint8_t* stage_buf = sbase + Cfg::OFF_EPI + ew * (16 * 32 * 2);
         int acc = 0;
         uint32_t aph = 0;
-        for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            const int tile = u / p.split;
+            const int sp = u - tile * p.split;
             const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
             const bool ok = __all_sync(0xffffffffu, wait_bounded(bar_accf + 8 * acc, aph, abort_flag,
                                                                  p.err, p.timeout_ns));
-            if (!ok) break;
+            if (!ok && p.split == 1) break;
             tc_fence_after();
             const float al = __ldg(p.alpha + tc.g);
             const int n0 = tc.nt * 128 + quad * 32;   // first of this warp's 32 weight rows
@@ -439,31 +471,92 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             // weight rows n0 + 8*(lane & 3) .. +7
             const int tr = lane >> 2, tq = lane & 3;
             const bool n_ok = n0 + 8 * tq < p.N;
+            __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stage_buf);
+            if (p.split == 1) {
 #pragma unroll 1
-            for (int c = 0; c < TT_MAX / 16; ++c) {
-                if (c * 16 >= tc.w) break;
-                uint32_t r[16];
-                tmem_ld_32x32b_x16(tbase + c * 16, r);
-                tmem_wait_ld();
-                // lane = weight row n0 + lane; column t = token; transpose via
-                // shared memory into [token][32 rows] bf16
-                __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stage_buf);
+                for (int c = 0; c < TT_MAX / 16; ++c) {
+                    if (c * 16 >= tc.w) break;
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(tbase + c * 16, r);
+                    tmem_wait_ld();
+                    // lane = weight row n0 + lane; column t = token; transpose via
+                    // shared memory into [token][32 rows] bf16
 #pragma unroll
-                for (int t = 0; t < 16; ++t) sb[t * 32 + lane] = __float2bfloat16_rn(al * __uint_as_float(r[t]));
-                __syncwarp();
+                    for (int t = 0; t < 16; ++t) sb[t * 32 + lane] = __float2bfloat16_rn(al * __uint_as_float(r[t]));
+                    __syncwarp();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int t = tr + 8 * h;
-                    const int tok = tc.t0 + c * 16 + t;
-                    const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + t * 64 + tq * 16);
-                    if (tok < t_end && n_ok)
-                        *reinterpret_cast<uint4*>(p.C + ((size_t)tc.g * p.M_max + tok) * p.N + n0 + 8 * tq) = v;
+                    for (int h = 0; h < 2; ++h) {
+                        const int t = tr + 8 * h;
+                        const int tok = tc.t0 + c * 16 + t;
+                        const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + t * 64 + tq * 16);
+                        if (tok < t_end && n_ok)
+                            *reinterpret_cast<uint4*>(p.C + ((size_t)tc.g * p.M_max + tok) * p.N + n0 + 8 * tq) = v;
+                    }
+                    __syncwarp();
                 }
+                tc_fence_before();
                 __syncwarp();
+                if (lane == 0) mbar_arrive(bar_acce + 8 * acc);
+            } else {
+                // split-K.  The 4 epilogue warps pass the same named-barrier
+                // sequence on every unit, even after a timeout (then they skip
+                // the work), and leave the loop together on a flag set under
+                // the barrier, so no warp can wait on a barrier another left.
+                if (ok) {
+                    // leave this range's fp32 partial, [column][128 rows]
+                    float* part = p.ws_part + ((size_t)tile * p.split + sp) * (TT_MAX * 128) + quad * 32 + lane;
+#pragma unroll 1
+                    for (int c = 0; c < TT_MAX / 16; ++c) {
+                        if (c * 16 >= tc.w) break;
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(tbase + c * 16, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) part[(c * 16 + t) * 128] = __uint_as_float(r[t]);
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acce + 8 * acc);   // TMEM no longer needed
+                }
+                __threadfence();
+                named_barrier_sync(1, 128);                          // the 4 epilogue warps
+                if (ew == 0 && lane == 0) {
+                    const int stop = *abort_flag;
+                    *epi_stop = stop;
+                    *epi_flag = (!stop && atomicAdd(p.ws_cnt + tile, 1) == p.split - 1) ? 1 : 0;
+                }
+                named_barrier_sync(1, 128);
+                if (*epi_flag) {
+                    // the last range: sum all ranges' partials in range order
+                    __threadfence();
+                    const float* base_part = p.ws_part + (size_t)tile * p.split * (TT_MAX * 128) + quad * 32 + lane;
+#pragma unroll 1
+                    for (int c = 0; c < TT_MAX / 16; ++c) {
+                        if (c * 16 >= tc.w) break;
+#pragma unroll 4
+                        for (int t = 0; t < 16; ++t) {
+                            float acc_v = 0.f;
+                            for (int r2 = 0; r2 < p.split; ++r2)
+                                acc_v += __ldcg(base_part + (size_t)r2 * (TT_MAX * 128) + (c * 16 + t) * 128);
+                            sb[t * 32 + lane] = __float2bfloat16_rn(al * acc_v);
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int t = tr + 8 * h;
+                            const int tok = tc.t0 + c * 16 + t;
+                            const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + t * 64 + tq * 16);
+                            if (tok < t_end && n_ok)
+                                *reinterpret_cast<uint4*>(p.C + ((size_t)tc.g * p.M_max + tok) * p.N + n0 + 8 * tq) = v;
+                        }
+                        __syncwarp();
+                    }
+                    if (ew == 0 && lane == 0) p.ws_cnt[tile] = 0;   // ready for the next call
+                }
+                const bool stop = *epi_stop != 0;
+                named_barrier_sync(1, 128);   // epi_flag / epi_stop are reused by the next unit
+                if (stop) break;
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar_acce + 8 * acc);
             if (++acc == Cfg::ACC_BUFS) { acc = 0; aph ^= 1u; }
         }
     }

@@ -261,9 +261,33 @@ int nvfp4_prepare_weights(const void* B, const void* B_sf, int G, int N, int K, 
     return cuda_status(cudaGetLastError());
 }
 
-int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B, const void* B_sf,
-                                 const float* alpha, const int* masked_m, void* C, int G, int M_max,
-                                 int N, int K, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Upper bound of the decode kernel's tiles (every expert full) and the
+// split-K workspace layout: fp32 partials [tiles][split][32][128], then one
+// int counter per tile.
+long long decode_tile_bound(int G, int M_max, int N) {
+    return (long long)G * ((M_max + kNarrowTT - 1) / kNarrowTT) * ((N + 127) / 128);
+}
+
+size_t splitk_part_bytes(long long tiles, int split) {
+    return (size_t)tiles * split * kNarrowTT * 128 * sizeof(float);
+}
+
+int auto_split(DeviceState* d, long long tiles, int K) {
+    const int ks = K / 256;
+    long long s = tiles > 0 ? d->sms / tiles : 1;
+    if (s < 1) s = 1;
+    if (s > ks) s = ks;
+    if (s > 16) s = 16;
+    return (int)s;
+}
+
+int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf, const float* alpha,
+                const int* masked_m, void* C, int G, int M_max, int N, int K, int split,
+                float* ws_part, int* ws_cnt, void* stream) {
     if (!A || !A_sf || !B || !B_sf || !alpha || !masked_m || !C) return NVFP4GG_ERR_NULL;
     int rc = check_gemm_shape(G, M_max, N, K);
     if (rc != NVFP4GG_OK) return rc;
@@ -292,10 +316,68 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
     p.NT = (N + 127) / 128;
     p.KS = K / 256;
     p.timeout_ns = g_timeout_ns;
+    p.split = 1;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (narrow && split > 1) {
+        const long long tiles = decode_tile_bound(G, M_max, N);
+        if (tiles * split >= (1LL << 31)) return NVFP4GG_ERR_SHAPE;
+        if (cudaMemsetAsync(ws_cnt, 0, (size_t)tiles * sizeof(int), st) != cudaSuccess)
+            return NVFP4GG_ERR_CUDA;
+        p.split = split;
+        p.ws_part = ws_part;
+        p.ws_cnt = ws_cnt;
+    }
     if (narrow) return launch_variant<kNarrowTT, kNarrowStages>(d, 0, p, st);
     if (pair) return launch_pair_variant<kPairTT, kPairStages>(d, 2, p, st);
     return launch_variant<kWideTT, kWideStages>(d, 1, p, st);
+}
+
+}  // namespace
+
+extern "C" {
+
+int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B, const void* B_sf,
+                                 const float* alpha, const int* masked_m, void* C, int G, int M_max,
+                                 int N, int K, void* stream) {
+    return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr, nullptr,
+                       stream);
+}
+
+size_t nvfp4_splitk_workspace_bytes(int G, int M_max, int N, int K, int split_k) {
+    if (check_gemm_shape(G, M_max, N, K) != NVFP4GG_OK || split_k < 0 || split_k > 16) return 0;
+    if (M_max > 64) return 16;   // prefill shapes run unsplit: no workspace needed
+    const long long tiles = decode_tile_bound(G, M_max, N);
+    const int s = split_k == 0 ? 16 : split_k;
+    return ((splitk_part_bytes(tiles, s) + 255) & ~(size_t)255) + (size_t)tiles * sizeof(int);
+}
+
+int nvfp4_grouped_gemm_nt_masked_splitk(const void* A, const void* A_sf, const void* B,
+                                        const void* B_sf, const float* alpha, const int* masked_m,
+                                        void* C, int G, int M_max, int N, int K, int split_k,
+                                        void* workspace, size_t workspace_bytes, void* stream) {
+    if (!workspace) return NVFP4GG_ERR_NULL;
+    if (split_k < 0 || split_k > 16) return NVFP4GG_ERR_SHAPE;
+    int rc = check_gemm_shape(G, M_max, N, K);
+    if (rc != NVFP4GG_OK) return rc;
+    if (!aligned(workspace, 256)) return NVFP4GG_ERR_ALIGN;
+    if (M_max > 64)
+        return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr,
+                           nullptr, stream);
+    int split = split_k;
+    if (split == 0) {
+        DeviceState* d = nullptr;
+        if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
+        split = auto_split(d, decode_tile_bound(G, M_max, N), K);
+    }
+    if (split > K / 256) split = K / 256;
+    if (split < 1) split = 1;
+    const long long tiles = decode_tile_bound(G, M_max, N);
+    const size_t part = (splitk_part_bytes(tiles, split) + 255) & ~(size_t)255;
+    if (workspace_bytes < part + (size_t)tiles * sizeof(int)) return NVFP4GG_ERR_SHAPE;
+    float* ws_part = static_cast<float*>(workspace);
+    int* ws_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + part);
+    return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, split, ws_part, ws_cnt,
+                       stream);
 }
 
 size_t nvfp4_host_staging_bytes(int G, int M_max, int N, int K) {

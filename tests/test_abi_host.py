@@ -102,6 +102,23 @@ def test_host_variant_argument_checks(lib):
     assert f(*a) == binding.ERR_ALIGN
 
 
+def test_splitk_argument_checks(lib):
+    f = lib.nvfp4_grouped_gemm_nt_masked_splitk
+    need = binding.nvfp4_splitk_workspace_bytes(4, 16, 256, 512, 2)
+    tiles = 4 * 1 * 2
+    assert need == (tiles * 2 * 32 * 128 * 4 + 255) // 256 * 256 + tiles * 4
+    assert binding.nvfp4_splitk_workspace_bytes(4, 16, 256, 512, 17) == 0
+    args = [FAKE] * 7 + [4, 16, 256, 512, 2, FAKE, need, None]
+    a = list(args); a[12] = None
+    assert f(*a) == binding.ERR_NULL
+    a = list(args); a[11] = 17
+    assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[12] = FAKE + 16
+    assert f(*a) == binding.ERR_ALIGN
+    a = list(args); a[13] = need - 1
+    assert f(*a) == binding.ERR_SHAPE
+
+
 def test_sm_cap_and_watchdog_argument_checks(lib):
     assert lib.nvfp4_gg_set_sm_count(-1) == binding.ERR_SHAPE
     assert lib.nvfp4_gg_set_sm_count(0) == binding.OK

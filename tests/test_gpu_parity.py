@@ -147,6 +147,37 @@ def test_full_size_sampled_pair_kernel(lib, key):
         lib.nvfp4_gg_set_pair_mode(False)
 
 
+def run_gpu_splitk(d, split_k):
+    from nvfp4_block_scaled_masked_gb300.device import Problem
+    from nvfp4_block_scaled_masked_gb300 import binding
+    cfg = d["cfg"]
+    prob = Problem(d)
+    nbytes = binding.nvfp4_splitk_workspace_bytes(cfg.G, cfg.M_max, cfg.N, cfg.K, split_k)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):      # deterministic: two calls give the same bits
+        prob.reset_C()
+        binding.nvfp4_grouped_gemm_nt_masked_splitk(prob.A, prob.A_sf, prob.B_prep, prob.B_sf_prep,
+                                                    prob.alpha, prob.masked_m, prob.C, cfg.G,
+                                                    cfg.M_max, cfg.N, cfg.K, split_k, ws, nbytes)
+        rc = binding.nvfp4_gg_check_error()
+        assert rc == 0, binding.status_string(rc)
+        outs.append(prob.C_bits())
+    np.testing.assert_array_equal(outs[0], outs[1])
+    return outs[0]
+
+
+@pytest.mark.parametrize("G,M_max,N,K,masked,split", [
+    (3, 16, 256, 768, [5, 0, 16], 2),           # 3 k-stages split 1 + 2
+    (2, 40, 144, 1280, [40, 7], 3),             # N tail, 2 token tiles, 5 stages split 1/2/2
+    (1, 8, 4096, 7168, [7], 0),                 # one expert: automatic split (all SMs)
+    (4, 64, 384, 512, [64, 33, 0, 1], 16),      # split capped at K/256 = 2
+])
+def test_splitk_decode(lib, G, M_max, N, K, masked, split):
+    d = W.generate(W.custom(G, M_max, N, K, masked_m=masked), seed=31 * G + K)
+    check_full(d, run_gpu_splitk(d, split))
+
+
 def test_c2_decode_full(lib):
     d = W.generate(W.CONFIGS["c2"])
     check_full(d, run_gpu(d))
