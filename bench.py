@@ -245,13 +245,15 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="c2", choices=sorted(W.CONFIGS))
+    ap.add_argument("--config", default="c2", choices=sorted(W.CONFIGS) + sorted(W.EXTRA))
+    ap.add_argument("--splitk", type=int, default=-1,
+                    help="time nvfp4_grouped_gemm_nt_masked_splitk with this split (0 = automatic)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    cfg = W.CONFIGS[args.config]
+    cfg = W.lookup(args.config)
     ws, rank, local = dist_setup()
 
     if args.impl == "reference":
@@ -288,8 +290,19 @@ def main():
     prob.raw_B = prob.raw_Bsf = None
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    if args.splitk >= 0:
+        splitk_bytes = binding.nvfp4_splitk_workspace_bytes(cfg.G, cfg.M_max, cfg.N, cfg.K,
+                                                            args.splitk)
+        splitk_ws = torch.empty(splitk_bytes, dtype=torch.uint8, device="cuda")
+
+        def run_step():
+            binding.nvfp4_grouped_gemm_nt_masked_splitk(
+                prob.A, prob.A_sf, prob.B_prep, prob.B_sf_prep, prob.alpha, prob.masked_m, prob.C,
+                cfg.G, cfg.M_max, cfg.N, cfg.K, args.splitk, splitk_ws, splitk_bytes)
+    else:
+        run_step = prob.run
     for i in range(args.warmup):
-        prob.run()
+        run_step()
     if binding.nvfp4_gg_check_error() != 0:
         raise RuntimeError("device error during warm-up")
 
@@ -306,7 +319,7 @@ def main():
     for i in range(args.steps):
         flush_l2(flush, i)
         starts[i].record(stream)
-        prob.run()
+        run_step()
         ends[i].record(stream)
     torch.cuda.synchronize()
     if ws > 1:
@@ -363,6 +376,8 @@ def main():
         "algorithmic_gbs": gbs, "weight_gbs": wgbs,
         "prepare_weights_ms": statistics.median(prep_ms),
         "gpu_launches": args.steps,
+        "entry_point": ("nvfp4_grouped_gemm_nt_masked_splitk(split_k=%d)" % args.splitk
+                        if args.splitk >= 0 else "nvfp4_grouped_gemm_nt_masked"),
         "wall_s_timed_region": wall,
         "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
     }

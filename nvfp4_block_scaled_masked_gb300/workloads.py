@@ -71,6 +71,22 @@ CONFIGS = {
 }
 
 
+# Extra workloads beyond the five above (not benchmark headlines): a decode
+# call whose experts are all empty (the fixed cost of a call), and one with a
+# single non-empty expert, where the unsplit kernel has only 32 weight tiles
+# for the GPU's SMs (the case split-K is for).
+EXTRA = {
+    "x0": Config("x0", "decode GEMM1 all experts empty G=32 N=4096 K=7168", 32, 16, 4096, 7168,
+                 "fixed", masked_list=(0,) * 32),
+    "x1": Config("x1", "decode GEMM1 one expert G=1 masked_m=7 N=4096 K=7168", 1, 16, 4096, 7168,
+                 "fixed", masked_list=(7,)),
+}
+
+
+def lookup(key: str) -> Config:
+    return CONFIGS[key] if key in CONFIGS else EXTRA[key]
+
+
 def custom(G, M_max, N, K, masked_m=None, key="c0", alpha_one=False) -> Config:
     """An ad-hoc config (tests): masked_m fixed if given, else uniform 0..M_max."""
     if masked_m is not None:
