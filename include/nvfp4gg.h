@@ -25,8 +25,9 @@
  *   C:    bf16, round to nearest even.
  *
  * Conventions for every call:
- *   - All buffers are owned by the caller.  The library allocates no device
- *     memory in any call.
+ *   - All buffers are owned by the caller, except the static scratch of
+ *     nvfp4_grouped_gemm_nt_masked_splitk_noalloc.  The library allocates no
+ *     device memory in any call.
  *   - Device pointers must be 16-byte aligned (alpha and masked_m: 4-byte).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream) and never synchronise the host, except
@@ -53,7 +54,8 @@ typedef enum {
     NVFP4GG_ERR_ARCH = -4,      /* the current device is not compute capability 10.3 */
     NVFP4GG_ERR_CUDA = -5,      /* a CUDA runtime/driver call failed                 */
     NVFP4GG_ERR_TIMEOUT = -6,   /* a device-side wait ran past its limit (error word) */
-    NVFP4GG_ERR_MASK = -7       /* masked_m[g] outside [0, M_max] seen on the device  */
+    NVFP4GG_ERR_MASK = -7,      /* masked_m[g] outside [0, M_max] seen on the device  */
+    NVFP4GG_ERR_SCRATCH = -8    /* split needs more than the library's static scratch */
 } nvfp4gg_status;
 
 /* Shape limits of nvfp4_grouped_gemm_nt_masked. */
@@ -131,6 +133,48 @@ int nvfp4_grouped_gemm_nt_masked_splitk(const void* A, const void* A_sf, const v
                                         const void* B_sf, const float* alpha, const int* masked_m,
                                         void* C, int G, int M_max, int N, int K, int split_k,
                                         void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Split-K without a caller workspace.  This entry point has no counterpart
+ * on the pages that define the operation; it exists for callers that cannot
+ * allocate device memory at call time: a serving loop that has handed all of
+ * HBM to weights and KV cache before it starts, code that must not hit the
+ * device-wide synchronisation of cudaFree, or a C caller with no device
+ * allocator of its own.  It allocates nothing.  It computes exactly what
+ * nvfp4_grouped_gemm_nt_masked_splitk computes with the same split (the same
+ * kernel and reduction order, so the same bits), using a scratch buffer that
+ * is a static __device__ array of the library, reserved once per device when
+ * the library's module is loaded there:
+ *   NVFP4GG_NOALLOC_MAX_SLOTS fp32 partial tiles of 32 x 128 (16 KiB each,
+ *   4 MiB in all) plus one int arrival counter per slot (1 KiB).
+ * A split call uses tiles x split slots, tiles = G * ceil(M_max/32) *
+ * ceil(N/128) (every expert counted full).
+ *   split_k  0: the automatic split of the workspace variant, lowered until
+ *               tiles x split fits the scratch (1 = unsplit when even 2 does
+ *               not fit);
+ *            1: unsplit, the scratch is not touched;
+ *            2..16: that split (capped at K/256); NVFP4GG_ERR_SCRATCH, with
+ *               nothing launched, when tiles x split exceeds
+ *               NVFP4GG_NOALLOC_MAX_SLOTS.
+ * With M_max > 64 the call runs unsplit.  Other arguments as in
+ * nvfp4_grouped_gemm_nt_masked.
+ * State: the partials need no initial value; the counters must be zero when
+ * a split kernel starts.  They are zero when the module loads, each call
+ * clears the ones it uses with an asynchronous memset on `stream` before its
+ * launch, and the kernel leaves them at zero.
+ * The first call on a device looks up the scratch's device address
+ * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit: make one
+ * call on each device before capturing a stream.
+ * Calls that may run at the same time on one device (different streams, or
+ * host threads that do not order their calls) share the scratch and race on
+ * it: their results are undefined.  Order them on one stream, or give each
+ * stream its own workspace through nvfp4_grouped_gemm_nt_masked_splitk.
+ */
+#define NVFP4GG_NOALLOC_MAX_SLOTS 256
+int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(const void* A, const void* A_sf, const void* B,
+                                                const void* B_sf, const float* alpha,
+                                                const int* masked_m, void* C, int G, int M_max,
+                                                int N, int K, int split_k, void* stream);
 
 /*
  * End-to-end variant for callers whose activations live in host memory.

@@ -23,6 +23,7 @@ ERR_ARCH = -4
 ERR_CUDA = -5
 ERR_TIMEOUT = -6
 ERR_MASK = -7
+ERR_SCRATCH = -8
 
 # every symbol the header declares
 EXPORTS = (
@@ -31,6 +32,7 @@ EXPORTS = (
     "nvfp4_grouped_gemm_nt_masked",
     "nvfp4_splitk_workspace_bytes",
     "nvfp4_grouped_gemm_nt_masked_splitk",
+    "nvfp4_grouped_gemm_nt_masked_splitk_noalloc",
     "nvfp4_host_staging_bytes",
     "nvfp4_grouped_gemm_nt_masked_host",
     "nvfp4_gg_set_sm_count",
@@ -73,6 +75,8 @@ def load():
     lib.nvfp4_splitk_workspace_bytes.restype = sz
     lib.nvfp4_grouped_gemm_nt_masked_splitk.argtypes = [vp] * 7 + [i] * 5 + [vp, sz, vp]
     lib.nvfp4_grouped_gemm_nt_masked_splitk.restype = i
+    lib.nvfp4_grouped_gemm_nt_masked_splitk_noalloc.argtypes = [vp] * 7 + [i] * 5 + [vp]
+    lib.nvfp4_grouped_gemm_nt_masked_splitk_noalloc.restype = i
     lib.nvfp4_host_staging_bytes.argtypes = [i] * 4
     lib.nvfp4_host_staging_bytes.restype = sz
     lib.nvfp4_grouped_gemm_nt_masked_host.argtypes = [vp] * 7 + [i] * 4 + [vp, sz, vp]
@@ -154,6 +158,14 @@ def nvfp4_grouped_gemm_nt_masked_splitk(A, A_sf, B, B_sf, alpha, masked_m, C, G,
         _ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf), _ptr(alpha), _ptr(masked_m), _ptr(C),
         G, M_max, N, K, split_k, _ptr(workspace), workspace_bytes, _stream(stream)),
         "nvfp4_grouped_gemm_nt_masked_splitk")
+
+
+def nvfp4_grouped_gemm_nt_masked_splitk_noalloc(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max,
+                                                N, K, split_k, stream=None):
+    _check(load().nvfp4_grouped_gemm_nt_masked_splitk_noalloc(
+        _ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf), _ptr(alpha), _ptr(masked_m), _ptr(C),
+        G, M_max, N, K, split_k, _stream(stream)),
+        "nvfp4_grouped_gemm_nt_masked_splitk_noalloc")
 
 
 def nvfp4_host_staging_bytes(G, M_max, N, K) -> int:

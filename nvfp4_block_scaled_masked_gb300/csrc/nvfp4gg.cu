@@ -223,6 +223,8 @@ const char* nvfp4_gg_status_string(int s) {
         case NVFP4GG_ERR_CUDA: return "NVFP4GG_ERR_CUDA: a CUDA call failed";
         case NVFP4GG_ERR_TIMEOUT: return "NVFP4GG_ERR_TIMEOUT: a device-side wait ran out";
         case NVFP4GG_ERR_MASK: return "NVFP4GG_ERR_MASK: masked_m outside [0, M_max]";
+        case NVFP4GG_ERR_SCRATCH:
+            return "NVFP4GG_ERR_SCRATCH: tiles x split_k exceeds NVFP4GG_NOALLOC_MAX_SLOTS";
         default: return "unknown nvfp4gg status";
     }
 }
@@ -484,3 +486,73 @@ int nvfp4_gg_mma_peak_probe(int iters, int n, int ctas, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Split-K with a library-owned scratch (nvfp4_grouped_gemm_nt_masked_splitk_noalloc).
+// The scratch is a static device array, laid out like a caller workspace:
+// fp32 partials for NVFP4GG_NOALLOC_MAX_SLOTS (tile, K-range) slots, then one
+// int arrival counter per slot.  Every device that loads the module gets its
+// own copy, zero-initialised.
+
+namespace {
+
+constexpr size_t kNoAllocPartBytes =
+    (size_t)NVFP4GG_NOALLOC_MAX_SLOTS * kNarrowTT * 128 * sizeof(float);   // 4 MiB
+constexpr size_t kNoAllocBytes = kNoAllocPartBytes + NVFP4GG_NOALLOC_MAX_SLOTS * sizeof(int);
+static_assert(kNoAllocPartBytes % 256 == 0, "counters must start 256-byte aligned");
+
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+namespace {
+
+unsigned char* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of this device's scratch, looked up on the first call made
+// with the device current.
+int noalloc_scratch(unsigned char** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4GG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return NVFP4GG_ERR_CUDA;
+        g_noalloc_addr[dev] = static_cast<unsigned char*>(p);
+    }
+    *out = g_noalloc_addr[dev];
+    return NVFP4GG_OK;
+}
+
+}  // namespace
+
+extern "C" int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(
+    const void* A, const void* A_sf, const void* B, const void* B_sf, const float* alpha,
+    const int* masked_m, void* C, int G, int M_max, int N, int K, int split_k, void* stream) {
+    if (!A || !A_sf || !B || !B_sf || !alpha || !masked_m || !C) return NVFP4GG_ERR_NULL;
+    if (split_k < 0 || split_k > 16) return NVFP4GG_ERR_SHAPE;
+    int rc = check_gemm_shape(G, M_max, N, K);
+    if (rc != NVFP4GG_OK) return rc;
+    if (M_max > 64 || split_k == 1)
+        return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr,
+                           nullptr, stream);
+    const long long tiles = decode_tile_bound(G, M_max, N);
+    const long long slots = NVFP4GG_NOALLOC_MAX_SLOTS;
+    int split = split_k;
+    if (split > K / 256) split = K / 256;
+    if (split_k > 1 && split > 1 && tiles * split > slots) return NVFP4GG_ERR_SCRATCH;
+    if (split_k == 0) {
+        DeviceState* d = nullptr;
+        if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
+        split = auto_split(d, tiles, K);
+        if (tiles * split > slots) split = (int)(slots / tiles);
+    }
+    if (split <= 1)
+        return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr,
+                           nullptr, stream);
+    unsigned char* scratch = nullptr;
+    if ((rc = noalloc_scratch(&scratch)) != NVFP4GG_OK) return rc;
+    return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, split,
+                       reinterpret_cast<float*>(scratch),
+                       reinterpret_cast<int*>(scratch + kNoAllocPartBytes), stream);
+}

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for s in range(0, -8, -1):
+    for s in range(0, -9, -1):
         assert binding.status_string(s).startswith("NVFP4GG_")
     assert "unknown" in binding.status_string(42)
 
@@ -117,6 +117,31 @@ def test_splitk_argument_checks(lib):
     assert f(*a) == binding.ERR_ALIGN
     a = list(args); a[13] = need - 1
     assert f(*a) == binding.ERR_SHAPE
+
+
+def test_noalloc_splitk_argument_checks(lib):
+    """The static-scratch split-K call: bad arguments and splits that do not
+    fit its NVFP4GG_NOALLOC_MAX_SLOTS scratch slots are refused before any
+    CUDA call."""
+    f = lib.nvfp4_grouped_gemm_nt_masked_splitk_noalloc
+    slots = 256
+    # G=8, M_max=16, N=4096: 8 * 1 * 32 = 256 tiles
+    args = [FAKE] * 7 + [8, 16, 4096, 7168, 2, None]
+    a = list(args); a[0] = None
+    assert f(*a) == binding.ERR_NULL
+    a = list(args); a[11] = 17
+    assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[11] = -1
+    assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[10] = 7000          # K % 256 != 0
+    assert f(*a) == binding.ERR_SHAPE
+    assert 256 * 2 > slots
+    assert f(*args) == binding.ERR_SCRATCH
+    a = list(args); a[7] = 4; a[11] = 3     # 128 tiles x 3 > 256
+    assert f(*a) == binding.ERR_SCRATCH
+    a = list(args); a[7] = 1; a[9] = 16384; a[11] = 16   # 128 tiles x 16
+    assert f(*a) == binding.ERR_SCRATCH
+    assert "NOALLOC_MAX_SLOTS" in binding.status_string(binding.ERR_SCRATCH)
 
 
 def test_sm_cap_and_watchdog_argument_checks(lib):
