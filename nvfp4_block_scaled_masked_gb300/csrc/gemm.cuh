@@ -10,18 +10,21 @@
 // 128-row tensor-core tile even for decode-sized masked_m, and a ragged
 // masked_m wastes at most 15 token columns per tile.
 //
-// Roles (288 threads).  An asynchronous instruction (TMA copy, mbarrier
+// Roles (352 threads).  An asynchronous instruction (TMA copy, mbarrier
 // operation, tcgen05 copy/MMA/commit) occupies its issuing thread for tens of
-// cycles, so the per-stage work is spread over several issuing threads:
+// cycles (hundreds under load), so the per-stage work is spread over several
+// issuing threads:
 //   warp 0      weight producer (one lane): bulk copies of the 16 KB weight
 //               tile and its 2 KB scale atoms into the shared ring.
 //   warp 1      TMEM owner; MMA thread (one lane): 4 x tcgen05.mma (K = 64
 //               each) per stage, commit of the stage back to the producers.
 //   warp 2      token producer (one lane): one tiled TMA for the w token rows
 //               and one for their scale rows (a tensor map per width w).
-//   warps 3, 4  scale warps (even / odd stages): regroup the token scales
-//               into MMA atoms (all lanes), copy weight and token scale atoms
-//               to TMEM (one lane), commit them to the MMA thread.
+//   warps 3, 4, 9, 10  scale warps, one per TMEM lane quarter: every stage,
+//               each lane loads its scale words from shared memory and the
+//               warp writes them into its quarter with tcgen05.st (no
+//               tcgen05.cp: one thread issuing a dozen copies per stage was
+//               measured to be the bound of compute-bound tiles).
 //   warps 5..8  epilogue: tcgen05.ld of the fp32 accumulator (lane = n,
 //               column = token), x alpha[g], bf16 round-to-nearest, a per-warp
 //               shared-memory transpose, 16-byte stores of rows m < masked_m[g].
@@ -30,10 +33,12 @@
 // token tiles of that expert, and experts with masked_m = 0 contribute none.
 //
 // Scale factors in TMEM: the MMA reads the scale of operand row r from TMEM
-// lane r % 32 (any quarter), column base + r / 32, byte = 16-element K block;
-// the base must be a multiple of 4 columns.  A 512-byte "atom" of 32 rows x
-// 16 bytes (row i: rows i, i+32, i+64, i+96 x 4 K blocks) copied with
-// tcgen05.cp.32x128b.warpx4 lands exactly there.
+// lane r % 32 (every lane quarter holds the same words), column
+// base + r / 32, byte = 16-element K block; the base must be a multiple of 4
+// columns.  So lane i, column base + c holds the 4 scale bytes of one K chunk
+// of 64 for row 32c + i: for the weights that is word c of row i of a
+// 512-byte atom of the prepared scales, for the tokens word (K chunk) of the
+// plain scale row 32c + i loaded by TMA.
 //
 // Every wait on an mbarrier is bounded (time limit in the parameters); on
 // expiry the waiter records NVFP4GG_ERR_TIMEOUT in the error word, raises a
@@ -47,7 +52,7 @@
 namespace nvfp4gg {
 
 constexpr int kGroupsMax = NVFP4GG_MAX_GROUPS;
-constexpr int kThreads = 288;
+constexpr int kThreads = 352;
 constexpr int kMaxWidths = 16;   // token tile widths 16, 32, ..., 256 rows
 
 struct GemmParams {
@@ -88,9 +93,7 @@ struct KCfg {
     static constexpr int T_TILE = TT_MAX * 128;      // TT_MAX token rows x 256 codes
     static constexpr int WSF_STAGE = 4 * 512;        // 4 weight-scale atoms
     static constexpr int TSF_PLAIN = TT_MAX * 16;    // token scales, 16 bytes per row
-    static constexpr int NA = (TT_MAX + 127) / 128;  // token atoms per MMA
-    static constexpr int JMAX = TT_MAX / 32 < 4 ? TT_MAX / 32 : 4;
-    static constexpr int TSF_ATOMS = 4 * NA * 512;
+    static constexpr int NA = (TT_MAX + 127) / 128;  // 128-row token groups per MMA
     static constexpr int ACC_BUFS = 2;
     static constexpr int SFW_COLS = 16;              // 4 MMAs x 4 columns
     static constexpr int SFT_COLS = 16 * NA;
@@ -109,12 +112,11 @@ struct KCfg {
     static constexpr int OFF_T = OFF_W + STAGES * W_TILE;
     static constexpr int OFF_WSF = OFF_T + STAGES * T_TILE;
     static constexpr int OFF_TSFP = OFF_WSF + STAGES * WSF_STAGE;
-    static constexpr int OFF_TSFA = OFF_TSFP + STAGES * TSF_PLAIN;
-    static constexpr int OFF_EPI = OFF_TSFA + STAGES * TSF_ATOMS;   // 4 warps x 16 tokens x 32 n bf16
+    static constexpr int OFF_EPI = OFF_TSFP + STAGES * TSF_PLAIN;   // 4 warps x 16 tokens x 32 n bf16
     static constexpr int EPI_BYTES = 4 * 16 * 32 * 2;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    // full, sfull, empty, sfready per stage; acc full/empty per buffer; three drains
-    static constexpr int NUM_BARS = 4 * STAGES + 2 * ACC_BUFS + 3;
+    // full, sfull, empty, sfready per stage; acc full/empty per buffer; MMA drain
+    static constexpr int NUM_BARS = 4 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_TAB = (OFF_MISC + 16 + 15) & ~15;
     // cum[kGroupsMax + 1] (tile prefix), gm[kGroupsMax] (clamped masked_m)
@@ -198,11 +200,10 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
     const uint32_t bar_full = base + Cfg::OFF_BAR;               // operand tiles: 2 producers + bytes
     const uint32_t bar_sfull = bar_full + 8 * STAGES;            // scale rows: 2 producers + bytes
     const uint32_t bar_empty = bar_sfull + 8 * STAGES;           // MMA commit
-    const uint32_t bar_sfready = bar_empty + 8 * STAGES;         // scale warp commit
+    const uint32_t bar_sfready = bar_empty + 8 * STAGES;         // 4 scale warps
     const uint32_t bar_accf = bar_sfready + 8 * STAGES;          // MMA commit, last stage
     const uint32_t bar_acce = bar_accf + 8 * Cfg::ACC_BUFS;      // 4 epilogue warps
     const uint32_t bar_done = bar_acce + 8 * Cfg::ACC_BUFS;      // MMA thread's drain
-    const uint32_t bar_done2 = bar_done + 8;                     // scale warps' drains (2)
     uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     volatile int* epi_flag = reinterpret_cast<volatile int*>(misc + 2);   // split-K: last range
@@ -215,15 +216,13 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             mbar_init(bar_full + 8 * s, 2);
             mbar_init(bar_sfull + 8 * s, 2);
             mbar_init(bar_empty + 8 * s, 1);
-            mbar_init(bar_sfready + 8 * s, 1);
+            mbar_init(bar_sfready + 8 * s, 4);
         }
         for (int b = 0; b < Cfg::ACC_BUFS; ++b) {
             mbar_init(bar_accf + 8 * b, 1);
             mbar_init(bar_acce + 8 * b, 4);
         }
         mbar_init(bar_done, 1);
-        mbar_init(bar_done2, 1);
-        mbar_init(bar_done2 + 8, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -354,10 +353,11 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                 const uint32_t idesc = idesc_mxf4nvf4((uint32_t)tc.w);
                 const uint32_t d_tmem = tmem + acc * TT_MAX;
                 for (int ks = kb; ks < ke; ++ks) {
-                    // operand tiles landed (full) and both scale sets are in
-                    // TMEM (the scale warp commits after its copies)
-                    if (!wait_bounded(bar_full + 8 * s, ph, abort_flag, p.err, p.timeout_ns) ||
-                        !wait_bounded(bar_sfready + 8 * s, ph, abort_flag, p.err, p.timeout_ns)) {
+                    // both scale sets are in TMEM and the operand tiles have
+                    // landed: the four scale warps arrive after their stores,
+                    // one of them only after the stage's full barrier, so one
+                    // wait covers both (one wait less in the issuing thread)
+                    if (!wait_bounded(bar_sfready + 8 * s, ph, abort_flag, p.err, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
@@ -382,73 +382,71 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             volatile int no_abort = 0;
             wait_bounded(bar_done, 0, &no_abort, p.err, p.timeout_ns);
         }
-    } else if (warp == 3 || warp == 4) {
-        // ------------------------------------------ scale warps (even / odd stages)
-        const int parity = warp - 3;
+    } else if (warp == 3 || warp == 4 || warp == 9 || warp == 10) {
+        // ------------------------------- scale warps (one per TMEM lane quarter)
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         int s = 0;
         uint32_t ph = 0;
-        long long cnt = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const int tile = u / p.split;
             int kb, ke;
             k_range(u - tile * p.split, p.split, p.KS, kb, ke);
-            for (int ks = kb; ks < ke; ++ks, ++cnt) {
-                if ((int)(cnt & 1) == parity) {
-                    ok = __all_sync(0xffffffffu, wait_bounded(bar_sfull + 8 * s, ph, abort_flag,
+            for (int ks = kb; ks < ke; ++ks) {
+                ok = __all_sync(0xffffffffu, wait_bounded(bar_sfull + 8 * s, ph, abort_flag,
+                                                          p.err, p.timeout_ns));
+                if (!ok) break;
+                // The MMAs that read this stage's scale columns in the previous
+                // round completed before its loads were issued (empty barrier).
+                tc_fence_after();
+                // weights: column 4q + c = word c of row `lane` of atom q
+                const uint8_t* wsf = sbase + Cfg::OFF_WSF + s * Cfg::WSF_STAGE + lane * 16;
+                uint32_t w[16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(wsf + 512 * q);
+                    w[4 * q] = v.x;
+                    w[4 * q + 1] = v.y;
+                    w[4 * q + 2] = v.z;
+                    w[4 * q + 3] = v.w;
+                }
+                // tokens: column 4(q NA + a) + c = word q of plain row
+                // 128a + 32c + lane (rows past TT_MAX: zero, never read)
+                const uint8_t* plain = sbase + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN + lane * 16;
+                uint32_t t[16 * Cfg::NA];
+#pragma unroll
+                for (int a = 0; a < Cfg::NA; ++a) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (128 * a + 32 * c < TT_MAX)
+                            v = *reinterpret_cast<const uint4*>(plain + (128 * a + 32 * c) * 16);
+                        t[4 * (0 * Cfg::NA + a) + c] = v.x;
+                        t[4 * (1 * Cfg::NA + a) + c] = v.y;
+                        t[4 * (2 * Cfg::NA + a) + c] = v.z;
+                        t[4 * (3 * Cfg::NA + a) + c] = v.w;
+                    }
+                }
+                const uint32_t sfw = tmem_sf + s * Cfg::SF_COLS + lane_off;
+                tmem_st_32x32b_x16(sfw, w);
+#pragma unroll
+                for (int h = 0; h < Cfg::NA; ++h)
+                    tmem_st_32x32b_x16(sfw + Cfg::SFW_COLS + 16 * h, t + 16 * h);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                // warp 3 also waits for the stage's operand tiles, so that the
+                // completed sfready phase tells the MMA thread both
+                if (warp == 3) {
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar_full + 8 * s, ph, abort_flag,
                                                               p.err, p.timeout_ns));
                     if (!ok) break;
-                    // plain rows (token t: 4 words, one per MMA) -> per-MMA
-                    // atoms (row i: tokens i, i+32, i+64, i+96)
-                    const uint8_t* plain = sbase + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN;
-                    uint8_t* atoms = sbase + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
-#pragma unroll
-                    for (int a = 0; a < Cfg::NA; ++a) {
-                        uint4 v[4] = {};
-#pragma unroll
-                        for (int j = 0; j < Cfg::JMAX; ++j)
-                            if (128 * a + 32 * j < TT_MAX)
-                                v[j] = *reinterpret_cast<const uint4*>(plain + (128 * a + 32 * j + lane) * 16);
-                        *reinterpret_cast<uint4*>(atoms + (0 * Cfg::NA + a) * 512 + lane * 16) =
-                            make_uint4(v[0].x, v[1].x, v[2].x, v[3].x);
-                        *reinterpret_cast<uint4*>(atoms + (1 * Cfg::NA + a) * 512 + lane * 16) =
-                            make_uint4(v[0].y, v[1].y, v[2].y, v[3].y);
-                        *reinterpret_cast<uint4*>(atoms + (2 * Cfg::NA + a) * 512 + lane * 16) =
-                            make_uint4(v[0].z, v[1].z, v[2].z, v[3].z);
-                        *reinterpret_cast<uint4*>(atoms + (3 * Cfg::NA + a) * 512 + lane * 16) =
-                            make_uint4(v[0].w, v[1].w, v[2].w, v[3].w);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) {
-                        tc_fence_after();
-                        const uint32_t sfw = tmem_sf + s * Cfg::SF_COLS;
-                        const uint32_t sft = sfw + Cfg::SFW_COLS;
-                        const uint32_t wsf_s = base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE;
-                        const uint32_t tsfa_s = base + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
-                        const uint64_t c0 = sdesc_rows16(wsf_s), c1 = sdesc_rows16(wsf_s + 512);
-                        const uint64_t c2 = sdesc_rows16(wsf_s + 1024), c3 = sdesc_rows16(wsf_s + 1536);
-                        tmem_cp_32x128b_x4(sfw, c0);
-                        tmem_cp_32x128b_x4(sfw + 4, c1);
-                        tmem_cp_32x128b_x4(sfw + 8, c2);
-                        tmem_cp_32x128b_x4(sfw + 12, c3);
-#pragma unroll
-                        for (int q = 0; q < 4 * Cfg::NA; ++q)
-                            tmem_cp_32x128b_x4(sft + 4 * q, sdesc_rows16(tsfa_s + 512 * q));
-                        umma_commit(bar_sfready + 8 * s);
-                    }
-                    __syncwarp();
                 }
+                if (lane == 0) mbar_arrive(bar_sfready + 8 * s);
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
         }
-        // Drain this warp's scale copies before TMEM is freed.
-        if (lane == 0) {
-            umma_commit(bar_done2 + 8 * parity);
-            volatile int no_abort = 0;
-            wait_bounded(bar_done2 + 8 * parity, 0, &no_abort, p.err, p.timeout_ns);
-        }
-    } else if (warp >= 5) {
+    } else if (warp >= 5 && warp <= 8) {
         // ------------------------------------------------------------ epilogue
         const int ew = warp - 5;     // epilogue warp 0..3
         const int quad = warp & 3;   // TMEM lane quarter this warp may access
