@@ -16,8 +16,9 @@
 // issuing threads:
 //   warp 0      weight producer (one lane): bulk copies of the 16 KB weight
 //               tile and its 2 KB scale atoms into the shared ring.
-//   warp 1      TMEM owner; MMA thread (one lane): 4 x tcgen05.mma (K = 64
-//               each) per stage, commit of the stage back to the producers.
+//   warp 1      TMEM owner; MMA warp: walks the stages as a warp, one
+//               elected lane issues 4 x tcgen05.mma (K = 64 each) per stage
+//               and the commit of the stage back to the producers.
 //   warp 2      token producer (one lane): one tiled TMA for the w token rows
 //               and one for their scale rows (a tensor map per width w).
 //   warps 3, 4, 9, 10  scale warps, one per TMEM lane quarter: every stage,
@@ -334,54 +335,56 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             wait_bounded(bar_sfull + 8 * st, par, &no_abort, p.err, p.timeout_ns);
         }
     } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA thread
-        if (lane == 0) {
-            int s = 0;
-            uint32_t ph = 0;
-            int acc = 0;
-            uint32_t aph = 0;
-            bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                const int tile = u / p.split;
-                int kb, ke;
-                k_range(u - tile * p.split, p.split, p.KS, kb, ke);
-                const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
-                if (!wait_bounded(bar_acce + 8 * acc, aph ^ 1u, abort_flag, p.err, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                const uint32_t idesc = idesc_mxf4nvf4((uint32_t)tc.w);
-                const uint32_t d_tmem = tmem + acc * TT_MAX;
-                for (int ks = kb; ks < ke; ++ks) {
-                    // both scale sets are in TMEM and the operand tiles have
-                    // landed: the four scale warps arrive after their stores,
-                    // one of them only after the stage's full barrier, so one
-                    // wait covers both (one wait less in the issuing thread)
-                    if (!wait_bounded(bar_sfready + 8 * s, ph, abort_flag, p.err, p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t sfw = tmem_sf + s * Cfg::SF_COLS;
-                    const uint32_t sft = sfw + Cfg::SFW_COLS;
-                    const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_W + s * Cfg::W_TILE);
-                    const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_T + s * Cfg::T_TILE);
-                    const uint32_t acc_in = ks != kb;
+        // ------------------------------------------------------------ MMA warp
+        // All 32 lanes walk the loop, so every operand is warp-uniform; the
+        // elected lane issues the MMAs and the commits that track them.
+        int s = 0;
+        uint32_t ph = 0;
+        int acc = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+            const int tile = u / p.split;
+            int kb, ke;
+            k_range(u - tile * p.split, p.split, p.KS, kb, ke);
+            const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
+            ok = __all_sync(0xffffffffu, wait_bounded(bar_acce + 8 * acc, aph ^ 1u, abort_flag,
+                                                      p.err, p.timeout_ns));
+            if (!ok) break;
+            const uint32_t idesc = idesc_mxf4nvf4((uint32_t)tc.w);
+            const uint32_t d_tmem = tmem + acc * TT_MAX;
+            for (int ks = kb; ks < ke; ++ks) {
+                // both scale sets are in TMEM and the operand tiles have
+                // landed: the four scale warps arrive after their stores,
+                // one of them only after the stage's full barrier, so one
+                // wait covers both (one wait less in the issuing thread)
+                ok = __all_sync(0xffffffffu, wait_bounded(bar_sfready + 8 * s, ph, abort_flag,
+                                                          p.err, p.timeout_ns));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t sfw = tmem_sf + s * Cfg::SF_COLS;
+                const uint32_t sft = sfw + Cfg::SFW_COLS;
+                const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_W + s * Cfg::W_TILE);
+                const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_T + s * Cfg::T_TILE);
+                const uint32_t acc_in = ks != kb;
+                if (elect_one()) {
                     umma_mxf4nvf4(d_tmem, ad, bd, idesc, sfw, sft, acc_in);
                     umma_mxf4nvf4(d_tmem, ad + 2, bd + 2, idesc, sfw + 4, sft + 4 * Cfg::NA, 1u);
                     umma_mxf4nvf4(d_tmem, ad + 4, bd + 4, idesc, sfw + 8, sft + 8 * Cfg::NA, 1u);
                     umma_mxf4nvf4(d_tmem, ad + 6, bd + 6, idesc, sfw + 12, sft + 12 * Cfg::NA, 1u);
                     umma_commit(bar_empty + 8 * s);
                     if (ks == ke - 1) umma_commit(bar_accf + 8 * acc);
-                    if (++s == STAGES) { s = 0; ph ^= 1u; }
                 }
-                if (++acc == Cfg::ACC_BUFS) { acc = 0; aph ^= 1u; }
+                __syncwarp();
+                if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
-            // Drain the tensor pipe before TMEM is freed.
-            umma_commit(bar_done);
-            volatile int no_abort = 0;
-            wait_bounded(bar_done, 0, &no_abort, p.err, p.timeout_ns);
+            if (++acc == Cfg::ACC_BUFS) { acc = 0; aph ^= 1u; }
         }
+        // Drain the tensor pipe before TMEM is freed.
+        if (elect_one()) umma_commit(bar_done);
+        __syncwarp();
+        volatile int no_abort = 0;
+        wait_bounded(bar_done, 0, &no_abort, p.err, p.timeout_ns);
     } else if (warp == 3 || warp == 4 || warp == 9 || warp == 10) {
         // ------------------------------- scale warps (one per TMEM lane quarter)
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
