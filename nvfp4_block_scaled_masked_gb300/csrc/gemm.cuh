@@ -99,10 +99,15 @@ struct KCfg {
     static constexpr int SFW_COLS = 16;              // 4 MMAs x 4 columns
     static constexpr int SFT_COLS = 16 * NA;
     static constexpr int SF_COLS = SFW_COLS + SFT_COLS;
-    // One scale-factor TMEM region per ring stage: a region is rewritten only
-    // after the stage's full barrier of the next round, i.e. after the MMAs
-    // that read it completed.
-    static constexpr int TMEM_NEED = ACC_BUFS * TT_MAX + STAGES * SF_COLS;
+    // Scale-factor TMEM regions, used round-robin by stage count.  With one
+    // region per ring stage a region is rewritten only after the stage's next
+    // full barrier, i.e. after the MMAs that read it completed.  Where TMEM
+    // holds fewer (wide token tiles), the scale warps wait for those MMAs
+    // (the empty barrier of the stage that last used the region).
+    static constexpr int SF_FIT = (512 - ACC_BUFS * TT_MAX) / SF_COLS;
+    static constexpr int SF_BUFS = SF_FIT < STAGES ? SF_FIT : STAGES;
+    static_assert(SF_BUFS >= 2, "TMEM budget");
+    static constexpr int TMEM_NEED = ACC_BUFS * TT_MAX + SF_BUFS * SF_COLS;
     // Scale-factor operands of tcgen05.mma are addressed in groups of 4 TMEM
     // columns: every scale address below is a multiple of 4 columns.
     static_assert(TT_MAX % 4 == 0 && SF_COLS % 4 == 0 && SFW_COLS % 4 == 0, "SF alignment");
@@ -274,12 +279,13 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
     const uint32_t tmem = misc[0];
     const int total = cum[p.G];
     const int units = total * p.split;   // (tile, K range) work units
-    // TMEM map: accumulators [0, ACC_BUFS*TT_MAX), then one region per stage
-    // of 16 weight-scale + 16*NA token-scale columns
+    // TMEM map: accumulators [0, ACC_BUFS*TT_MAX), then SF_BUFS regions of 16
+    // weight-scale + 16*NA token-scale columns
     const uint32_t tmem_sf = tmem + Cfg::ACC_BUFS * TT_MAX;
 
-    if ((warp == 0 || warp == 2) && lane == 0) {
+    if (warp == 0 || warp == 2) {
         // ------------------------------------------- producers (weights / tokens)
+        // As the MMA warp: the warp walks the stages, the elected lane issues.
         const bool weights = warp == 0;
         const uint64_t pol_stream = policy_evict_first();
         int s = 0;
@@ -296,15 +302,15 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             const uint8_t* wsf_tile = p.wsf + wtile * Cfg::WSF_STAGE;
             const int box = (tc.w >> 4) - 1;   // tensor map of this token width
             for (int ks = kb; ks < ke; ++ks) {
-                if (!wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort_flag, p.err, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
+                ok = __all_sync(0xffffffffu, wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort_flag,
+                                                          p.err, p.timeout_ns));
+                if (!ok) break;
                 // scales first (small: the scale warps start on them while the
                 // operand tiles are still in flight), then the operand tile
                 const uint32_t fb = bar_full + 8 * s;
                 const uint32_t sb = bar_sfull + 8 * s;
-                if (weights) {
+                if (!elect_one()) {
+                } else if (weights) {
                     mbar_arrive_expect_tx(sb, Cfg::WSF_STAGE);
                     bulk_load_hint(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE,
                                    wsf_tile + (size_t)ks * Cfg::WSF_STAGE, Cfg::WSF_STAGE, sb,
@@ -320,6 +326,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                     tma_load_3d(base + Cfg::OFF_T + s * Cfg::T_TILE, &p.tm_a[box], fb, ks * 128,
                                 tc.t0, tc.g);
                 }
+                __syncwarp();
                 ++issued;
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
@@ -340,6 +347,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         // elected lane issues the MMAs and the commits that track them.
         int s = 0;
         uint32_t ph = 0;
+        int r = 0;   // scale region
         int acc = 0;
         uint32_t aph = 0;
         bool ok = true;
@@ -362,7 +370,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                                                           p.err, p.timeout_ns));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t sfw = tmem_sf + s * Cfg::SF_COLS;
+                const uint32_t sfw = tmem_sf + r * Cfg::SF_COLS;
                 const uint32_t sft = sfw + Cfg::SFW_COLS;
                 const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_W + s * Cfg::W_TILE);
                 const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_T + s * Cfg::T_TILE);
@@ -377,6 +385,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                 }
                 __syncwarp();
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
+                if (++r == Cfg::SF_BUFS) r = 0;
             }
             if (++acc == Cfg::ACC_BUFS) { acc = 0; aph ^= 1u; }
         }
@@ -390,6 +399,8 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         int s = 0;
         uint32_t ph = 0;
+        int r = 0;              // scale region
+        long long cnt = 0;      // stages walked
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const int tile = u / p.split;
@@ -399,8 +410,18 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                 ok = __all_sync(0xffffffffu, wait_bounded(bar_sfull + 8 * s, ph, abort_flag,
                                                           p.err, p.timeout_ns));
                 if (!ok) break;
-                // The MMAs that read this stage's scale columns in the previous
-                // round completed before its loads were issued (empty barrier).
+                if (Cfg::SF_BUFS < STAGES && cnt >= Cfg::SF_BUFS) {
+                    // the MMAs of the stage that last used region r are done
+                    const long long prev = cnt - Cfg::SF_BUFS;
+                    ok = __all_sync(0xffffffffu,
+                                    wait_bounded(bar_empty + 8 * (int)(prev % STAGES),
+                                                 (uint32_t)((prev / STAGES) & 1), abort_flag,
+                                                 p.err, p.timeout_ns));
+                    if (!ok) break;
+                }
+                // (With a region per stage, the MMAs that read this stage's
+                // scale columns in the previous round completed before its
+                // loads were issued: empty barrier.)
                 tc_fence_after();
                 // weights: column 4q + c = word c of row `lane` of atom q
                 const uint8_t* wsf = sbase + Cfg::OFF_WSF + s * Cfg::WSF_STAGE + lane * 16;
@@ -430,7 +451,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                         t[4 * (3 * Cfg::NA + a) + c] = v.w;
                     }
                 }
-                const uint32_t sfw = tmem_sf + s * Cfg::SF_COLS + lane_off;
+                const uint32_t sfw = tmem_sf + r * Cfg::SF_COLS + lane_off;
                 tmem_st_32x32b_x16(sfw, w);
 #pragma unroll
                 for (int h = 0; h < Cfg::NA; ++h)
@@ -447,6 +468,8 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                 }
                 if (lane == 0) mbar_arrive(bar_sfready + 8 * s);
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
+                if (++r == Cfg::SF_BUFS) r = 0;
+                ++cnt;
             }
         }
     } else if (warp >= 5 && warp <= 8) {

@@ -201,10 +201,12 @@ int launch_pair_variant(DeviceState* d, int slot, const GemmParams& p, cudaStrea
 }
 
 // Decode-sized experts (M_max <= 64): token tiles of at most 32, a deep ring
-// for the weight stream.  Larger experts: token tiles of up to 160, so that a
-// prefill expert's rows usually fit one tile and its weights stream once.
+// for the weight stream.  Larger experts: token tiles of up to 192, so that a
+// prefill expert's rows usually fit one tile and its weights stream once, and
+// each MMA instruction carries 128 x 192 x 64 (the issuing warp's per-stage
+// cost, not the tensor pipe, bounds compute-heavy tiles).
 constexpr int kNarrowTT = 32, kNarrowStages = 8;
-constexpr int kWideTT = 160, kWideStages = 4;
+constexpr int kWideTT = 192, kWideStages = 4;
 // Larger experts with N a multiple of 256: CTA pairs (M = 256 per MMA),
 // token tiles of up to 160 split 80 + 80 rows, six ring stages.
 constexpr int kPairTT = 160, kPairStages = 6;

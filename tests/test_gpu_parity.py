@@ -114,6 +114,8 @@ def test_c1_poisoned_rows_ignored(lib):
     (2, 64, 256, 1024, [64, 31]),                           # narrow kernel, M_max = 64
     (4, 200, 272, 768, [200, 129, 128, 1]),                 # wide kernel, ragged widths
     (2, 256, 384, 512, [256, 255]),                         # wide kernel, 2 x 128 tiles
+    (2, 192, 256, 2048, [192, 177]),                        # wide kernel, full 192-row tile,
+                                                            # 8 stages over 2 scale regions
     (1, 1, 16, 256, [1]),                                   # minimum sizes
     (6, 24, 128, 256, [0, 0, 0, 0, 0, 0]),                  # every expert empty
 ])
