@@ -142,14 +142,16 @@ __device__ __forceinline__ void record_error(int* err, int code) {
 
 // Bounded wait for the phase of `bar` with parity `parity`.  Gives up when
 // the shared abort flag is raised by another role, or after timeout_ns, in
-// which case it records the timeout and raises the flag itself.
+// which case it records the timeout and raises the flag itself.  Between
+// checks the thread sleeps in try_wait (woken when the phase completes), so
+// waiting warps leave the issue slots to the working ones.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile int* abort_flag, int* err,
                                              unsigned long long timeout_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
         if ((it & 31u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > timeout_ns) {
