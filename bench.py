@@ -383,7 +383,7 @@ def main():
     }
     if cfg.key == "c5":
         peak = peaks["bf16"] * NOMINAL_FP4_OVER_BF16
-        probe = {n: mma_peak_tflops(n) for n in (256, 208)}
+        probe = {n: mma_peak_tflops(n) for n in (256, 192)}
         line["roofline"] = {"bound": "tensor", "achieved": tflops / ws, "peak": peak,
                             "unit": "TFLOP/s", "frac": tflops / ws / peak,
                             "traffic": profiled_traffic(cfg.key),
@@ -398,8 +398,10 @@ def main():
     line["e2e"] = {"value": counts["flops"] / (e2e_med / 1e3) / 1e12, "unit": UNIT,
                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                    "ms_per_step": e2e_med, "steps": args.e2e_steps,
-                   "how": "nvfp4_grouped_gemm_nt_masked_host: pinned host inputs -> device, GEMM, "
-                          "valid rows of C -> pinned host, stream sync; wall clock per step"}
+                   "how": "nvfp4_grouped_gemm_nt_masked_host on pinned host buffers: A and A_sf "
+                          "copied to the device, alpha and masked_m read and the valid rows of C "
+                          "written by the kernel in host memory, stream sync; wall clock per "
+                          "step (Python call included)"}
     line["clocks"] = sampler.summary()
 
     if rank == 0 and not args.no_cpu_baseline:

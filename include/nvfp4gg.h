@@ -184,9 +184,15 @@ int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(const void* A, const void* A_sf,
  *   h_C: HOST bf16 [G][M_max][N]; only rows m < h_masked_m[g] are written
  *   d_staging: DEVICE scratch of at least nvfp4_host_staging_bytes(...) bytes,
  *       16-byte aligned, owned by the caller
- * Copies the inputs host->device, runs the GEMM, copies the valid rows of C
- * device->host (one copy per non-empty expert), all on `stream`.  Returns
- * when the work is queued; synchronise `stream` before reading h_C.
+ * Copies h_A and h_A_sf host->device, runs the GEMM and delivers the valid
+ * rows of C, all on `stream`.  Buffers in pinned (page-locked) host memory,
+ * which the device can address, are used in place: the kernel reads h_alpha
+ * and h_masked_m directly, and its epilogue stores the valid rows of C
+ * straight into h_C (16-byte aligned) over the CPU-GPU link.  Pageable
+ * buffers go through d_staging instead: one copy each for alpha and
+ * masked_m, and one device->host copy of C per non-empty expert.  Returns
+ * when the work is queued; synchronise `stream` before reading h_C, and do
+ * not modify the inputs before then.
  */
 size_t nvfp4_host_staging_bytes(int G, int M_max, int N, int K);
 int nvfp4_grouped_gemm_nt_masked_host(const void* h_A, const void* h_A_sf,

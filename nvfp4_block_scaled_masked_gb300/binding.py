@@ -109,10 +109,20 @@ def _ptr(x):
     raise TypeError(f"cannot take the address of {type(x)}")
 
 
+_raw_stream = None
+
+
 def _stream(s):
     if s is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        global _raw_stream
+        if _raw_stream is None:
+            import torch
+            raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+            if raw is not None:
+                _raw_stream = lambda: raw(torch.cuda.current_device())
+            else:
+                _raw_stream = lambda: torch.cuda.current_stream().cuda_stream
+        return _raw_stream()
     if isinstance(s, int):
         return s
     return s.cuda_stream

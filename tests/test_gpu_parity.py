@@ -210,18 +210,26 @@ def test_watchdog_reports_timeout(lib):
     check_full(d, run_gpu(d))
 
 
-def test_host_buffer_entry_point_matches_device_path(lib):
-    """nvfp4_grouped_gemm_nt_masked_host: pinned host inputs in, valid rows of
-    C out; bit-identical to the device-buffer call, other host rows untouched."""
+@pytest.mark.parametrize("pinned_in,pinned_out", [(True, True), (False, False), (True, False)])
+def test_host_buffer_entry_point_matches_device_path(lib, pinned_in, pinned_out):
+    """nvfp4_grouped_gemm_nt_masked_host: host inputs in, valid rows of C out;
+    bit-identical to the device-buffer call, other host rows untouched.
+    Pinned buffers are used in place (alpha, masked_m read and C written by
+    the kernel); pageable ones go through the device staging buffer."""
     from nvfp4_block_scaled_masked_gb300.device import Problem
     cfg = W.custom(5, 40, 272, 512, masked_m=[40, 0, 17, 33, 1])
     d = W.generate(cfg, seed=77)
     prob = Problem(d)
     prob.run()
     want = prob.C_bits()
-    h = {k: torch.from_numpy(np.ascontiguousarray(d[k])).pin_memory() for k in ("A", "A_sf", "alpha")}
-    h["masked_m"] = torch.from_numpy(d["masked_m"].astype(np.int32)).pin_memory()
-    hC = torch.full((cfg.G, cfg.M_max, cfg.N), W.SENTINEL_BF16, dtype=torch.int16).pin_memory()
+
+    def host(arr, pinned):
+        t = torch.from_numpy(np.ascontiguousarray(arr))
+        return t.pin_memory() if pinned else t
+
+    h = {k: host(d[k], pinned_in) for k in ("A", "A_sf", "alpha")}
+    h["masked_m"] = host(d["masked_m"].astype(np.int32), pinned_in)
+    hC = host(np.full((cfg.G, cfg.M_max, cfg.N), W.SENTINEL_BF16, dtype=np.int16), pinned_out)
     nbytes = lib.nvfp4_host_staging_bytes(cfg.G, cfg.M_max, cfg.N, cfg.K)
     staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     for _ in range(2):
