@@ -248,6 +248,9 @@ def main():
     ap.add_argument("--config", default="c2", choices=sorted(W.CONFIGS) + sorted(W.EXTRA))
     ap.add_argument("--splitk", type=int, default=-1,
                     help="time nvfp4_grouped_gemm_nt_masked_splitk with this split (0 = automatic)")
+    ap.add_argument("--pair-mode", default="auto", choices=["auto", "on", "off"],
+                    help="prefill kernel family: CTA pairs (on), single CTAs (off), or the "
+                         "library's automatic choice")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -277,6 +280,7 @@ def main():
     stream = torch.cuda.current_stream()
 
     # one-time weight re-layout, timed separately (median of 5)
+    binding.nvfp4_gg_set_pair_mode({"off": 0, "on": 1, "auto": 2}[args.pair_mode])
     prob = Problem(d, keep_raw_weights=True)
     prep_ms = []
     for _ in range(5):
@@ -378,6 +382,7 @@ def main():
         "gpu_launches": args.steps,
         "entry_point": ("nvfp4_grouped_gemm_nt_masked_splitk(split_k=%d)" % args.splitk
                         if args.splitk >= 0 else "nvfp4_grouped_gemm_nt_masked"),
+        "pair_mode": args.pair_mode,
         "wall_s_timed_region": wall,
         "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
     }

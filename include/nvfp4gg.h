@@ -209,15 +209,19 @@ int nvfp4_grouped_gemm_nt_masked_host(const void* h_A, const void* h_A_sf,
 int nvfp4_gg_set_sm_count(int sm_count);
 
 /*
- * Kernel family for experts with M_max > 64 (prefill sizes).  enable = 0
- * (default): one CTA per 128 weight rows.  enable = 1: when N is a multiple
- * of 256, the two CTAs of a 2-CTA cluster share one MMA of 256 weight rows
- * (each CTA stages 128 weight rows and half of the token rows).  The pair
- * kernel is correct but currently slower on GB300 (the leading CTA's
- * operand loads land late), hence opt-in.  Results are equal up to fp32
- * summation order.  Process-wide.  NVFP4GG_ERR_SHAPE unless 0 or 1.
+ * Kernel family for experts with M_max > 64 (prefill sizes).
+ *   mode 0: one CTA per 128 weight rows.
+ *   mode 1: when N is a multiple of 256, the two CTAs of a 2-CTA cluster
+ *           share one MMA of 256 weight rows (each CTA stages 128 weight
+ *           rows and half of the token rows).
+ *   mode 2 (default): CTA pairs when N % 256 == 0 and M_max <= 256, else
+ *           one CTA per 128 weight rows.  Measured on GB300: pairs are
+ *           ~8 % faster on bandwidth-bound prefill shapes (few token tiles
+ *           per expert) and ~2 % slower on compute-heavy ones.
+ * Results are equal up to fp32 summation order.  Process-wide.
+ * NVFP4GG_ERR_SHAPE unless 0, 1 or 2.
  */
-int nvfp4_gg_set_pair_mode(int enable);
+int nvfp4_gg_set_pair_mode(int mode);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error

@@ -194,8 +194,14 @@ def nvfp4_gg_set_sm_count(sm_count: int):
     _check(load().nvfp4_gg_set_sm_count(sm_count), "nvfp4_gg_set_sm_count")
 
 
-def nvfp4_gg_set_pair_mode(enable: bool):
-    _check(load().nvfp4_gg_set_pair_mode(1 if enable else 0), "nvfp4_gg_set_pair_mode")
+PAIR_OFF, PAIR_ON, PAIR_AUTO = 0, 1, 2
+
+
+def nvfp4_gg_set_pair_mode(mode):
+    """0 / False: single-CTA tiles; 1 / True: CTA pairs where N % 256 == 0;
+    2: automatic (the library's default)."""
+    m = (1 if mode else 0) if isinstance(mode, bool) else int(mode)
+    _check(load().nvfp4_gg_set_pair_mode(m), "nvfp4_gg_set_pair_mode")
 
 
 def nvfp4_gg_check_error(stream=None) -> int:

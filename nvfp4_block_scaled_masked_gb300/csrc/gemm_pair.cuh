@@ -5,31 +5,33 @@
 //
 // The two CTAs of a 2-CTA cluster run one tcgen05 MMA of M = 256 weight rows
 // (128 per CTA: weight blocks 2*np and 2*np + 1) by N = w tokens, the token
-// rows split half per CTA.  Per CTA this halves the token bytes staged per
-// stage and the MMA / scale-copy instructions issued per FLOP, so six ring
-// stages fit in shared memory.
+// rows split half per CTA.  Per SM this halves the token bytes staged per
+// stage for the same MMA work, so a deeper ring fits in shared memory: the
+// single-CTA kernel is bound by how many bytes its 4-stage ring keeps in
+// flight against the load latency.
 //
-// Roles (352 threads, both CTAs unless noted):
-//   warp 0      weight producer: scale atoms (2 KB) then the 16 KB tile of
-//               this CTA's weight block, bulk copies.
-//   warp 1      TMEM (allocated for the pair).  Leader CTA: the MMA thread,
-//               4 pair MMAs per stage, multicast commit of the stage to both
-//               CTAs.  Peer CTA: relays "this stage's tiles landed" to the
-//               leader.
-//   warp 2      token producer: all w token scale rows, then this CTA's half
-//               of the w token rows (one TMA each).
-//   warps 3..6  scale warps, one per MMA of the stage: regroup the token
-//               scales of that MMA into atoms; in the peer CTA they then
-//               relay "ready" to the leader, in the leader they copy the
-//               weight and token scale atoms of both CTAs to TMEM (pair copy)
-//               and commit them to the MMA thread.
-//   warps 7..10 epilogue, as in the single-CTA kernel, on this CTA's 128
-//               weight rows; the peer's warps release the accumulator to the
-//               leader with remote arrives.
+// Roles (352 threads, both CTAs unless noted; as in the single-CTA kernel,
+// a role's warp walks the stages with warp-uniform values and an elected
+// lane issues the single-thread instructions):
+//   warps 0, 2        weight / token producers: the scale atoms (2 KB) then
+//                     the 16 KB tile of this CTA's weight block; all w token
+//                     scale rows then this CTA's half of the w token rows.
+//   warp 1            TMEM (allocated for the pair).  Leader CTA: the MMA
+//                     warp, 4 pair MMAs per stage, multicast commit of the
+//                     stage to both CTAs.  Peer CTA: idle.
+//   warps 3, 4, 9, 10 scale warps, one per TMEM lane quarter, in each CTA:
+//                     this CTA's weight scales and all token scales into its
+//                     own TMEM with tcgen05.st; then an arrive on the
+//                     leader's sfready barrier (8 arrivals: the peer's are
+//                     remote).  Warp 3 first waits for its CTA's operand
+//                     tiles, so one barrier tells the MMA warp everything.
+//   warps 5..8        epilogue, as in the single-CTA kernel, on this CTA's
+//                     128 weight rows; the peer's warps release the
+//                     accumulator to the leader with remote arrives.
 // Cross-CTA signals are relaxed remote mbarrier arrives (tens of cycles; a
 // release arrive costs hundreds).  Each reports an event the signalling
 // thread has already observed complete -- tiles landed (it waited on the TMA
-// barrier), scale atoms written (proxy fence after the stores), TMEM read
+// barrier), scale factors stored (tcgen05.wait::st), TMEM read
 // (tcgen05.wait::ld) -- and the receiver acts on it only through the tensor
 // core after seeing the arrive.  Every wait is bounded.
 #pragma once
@@ -48,8 +50,6 @@ struct PairCfg {
     static constexpr int WSF_STAGE = 4 * 512;
     static constexpr int TSF_PLAIN = TT_MAX * 16;       // all token scale rows
     static constexpr int NA = (TT_MAX + 127) / 128;
-    static constexpr int JMAX = TT_MAX / 32 < 4 ? TT_MAX / 32 : 4;
-    static constexpr int TSF_ATOMS = 4 * NA * 512;
     static constexpr int ACC_BUFS = 2;
     static constexpr int SFW_COLS = 16;
     static constexpr int SFT_COLS = 16 * NA;
@@ -68,13 +68,11 @@ struct PairCfg {
     static constexpr int OFF_T = OFF_W + STAGES * W_TILE;
     static constexpr int OFF_WSF = OFF_T + STAGES * T_TILE;
     static constexpr int OFF_TSFP = OFF_WSF + STAGES * WSF_STAGE;
-    static constexpr int OFF_TSFA = OFF_TSFP + STAGES * TSF_PLAIN;
-    static constexpr int OFF_EPI = OFF_TSFA + STAGES * TSF_ATOMS;
+    static constexpr int OFF_EPI = OFF_TSFP + STAGES * TSF_PLAIN;
     static constexpr int EPI_BYTES = 4 * 16 * 32 * 2;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    // full, sfull, empty, sfready, pfull, psf per stage; accf, acce per
-    // buffer; the MMA drain and 4 scale-warp drains
-    static constexpr int NUM_BARS = 6 * STAGES + 2 * ACC_BUFS + 5;
+    // full, sfull, empty, sfready per stage; accf, acce per buffer; the MMA drain
+    static constexpr int NUM_BARS = 4 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_TAB = (OFF_MISC + 16 + 15) & ~15;
     static constexpr int TAB_BYTES = (2 * kGroupsMax + 1) * 4;
@@ -108,10 +106,6 @@ __device__ __forceinline__ TileCoord decode_pair_tile(const int* cum, const int*
     return c;
 }
 
-__device__ __forceinline__ uint32_t word_of(const uint4& v, int q) {
-    return q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w;
-}
-
 template <int TT_MAX, int STAGES>
 __global__ void __launch_bounds__(kPairThreads, 1)
 gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
@@ -128,13 +122,10 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
     const uint32_t bar_full = base + Cfg::OFF_BAR;          // this CTA's tiles: 2 producers + bytes
     const uint32_t bar_sfull = bar_full + 8 * STAGES;       // this CTA's scale rows
     const uint32_t bar_empty = bar_sfull + 8 * STAGES;      // leader's multicast commit
-    const uint32_t bar_sfready = bar_empty + 8 * STAGES;    // leader: 4 scale-warp commits
-    const uint32_t bar_pfull = bar_sfready + 8 * STAGES;    // leader: peer's tiles landed (relay)
-    const uint32_t bar_psf = bar_pfull + 8 * STAGES;        // leader: peer's 4 scale warps ready
-    const uint32_t bar_accf = bar_psf + 8 * STAGES;         // leader's multicast commit
+    const uint32_t bar_sfready = bar_empty + 8 * STAGES;    // leader: 4 local + 4 peer scale warps
+    const uint32_t bar_accf = bar_sfready + 8 * STAGES;     // leader's multicast commit
     const uint32_t bar_acce = bar_accf + 8 * Cfg::ACC_BUFS; // leader: 4 local + 4 peer epilogue warps
     const uint32_t bar_done = bar_acce + 8 * Cfg::ACC_BUFS; // MMA drain
-    const uint32_t bar_done_sc = bar_done + 8;              // 4 scale-warp drains
     uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int* cum = reinterpret_cast<int*>(sbase + Cfg::OFF_TAB);
@@ -145,16 +136,13 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
             mbar_init(bar_full + 8 * s, 2);
             mbar_init(bar_sfull + 8 * s, 2);
             mbar_init(bar_empty + 8 * s, 1);
-            mbar_init(bar_sfready + 8 * s, 4);
-            mbar_init(bar_pfull + 8 * s, 1);
-            mbar_init(bar_psf + 8 * s, 4);
+            mbar_init(bar_sfready + 8 * s, 8);
         }
         for (int b = 0; b < Cfg::ACC_BUFS; ++b) {
             mbar_init(bar_accf + 8 * b, 1);
             mbar_init(bar_acce + 8 * b, 8);
         }
         mbar_init(bar_done, 1);
-        for (int q = 0; q < 4; ++q) mbar_init(bar_done_sc + 8 * q, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -207,7 +195,7 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
     const int ncl = gridDim.x >> 1;
     const uint32_t tmem_sf = tmem + Cfg::ACC_BUFS * TT_MAX;
 
-    if ((warp == 0 || warp == 2) && lane == 0) {
+    if (warp == 0 || warp == 2) {
         // ----------------------------------------------------------- producers
         const bool weights = warp == 0;
         const uint64_t pol_stream = policy_evict_first();
@@ -223,14 +211,13 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
             const uint8_t* wsf_tile = p.wsf + wtile * Cfg::WSF_STAGE;
             const int half = tc.w >> 1;
             for (int ks = 0; ks < p.KS; ++ks) {
-                if (!wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort_flag, p.err,
-                                          p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
+                ok = __all_sync(0xffffffffu, wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort_flag,
+                                                          p.err, p.timeout_ns));
+                if (!ok) break;
                 const uint32_t fb = bar_full + 8 * s;
                 const uint32_t sb = bar_sfull + 8 * s;
-                if (weights) {
+                if (!elect_one()) {
+                } else if (weights) {
                     mbar_arrive_expect_tx(sb, Cfg::WSF_STAGE);
                     bulk_load_hint(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE,
                                    wsf_tile + (size_t)ks * Cfg::WSF_STAGE, Cfg::WSF_STAGE, sb,
@@ -246,6 +233,7 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
                     tma_load_3d(base + Cfg::OFF_T + s * Cfg::T_TILE, &p.tm_a[(half >> 4) - 1], fb,
                                 ks * 128, tc.t0 + (int)rank * half, tc.g);
                 }
+                __syncwarp();
                 ++issued;
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
@@ -258,132 +246,129 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
             wait_bounded(bar_full + 8 * st, par, &no_abort, p.err, p.timeout_ns);
             wait_bounded(bar_sfull + 8 * st, par, &no_abort, p.err, p.timeout_ns);
         }
-    } else if (warp == 1 && lane == 0 && leader) {
-        // -------------------------------------------------- MMA thread (leader)
+    } else if (warp == 1 && leader) {
+        // ---------------------------------------------------- MMA warp (leader)
         int s = 0;
         uint32_t ph = 0;
+        int r = 0;   // scale region
         int acc = 0;
         uint32_t aph = 0;
-        long long cnt = 0;
         bool ok = true;
         for (int tile = cid; tile < total && ok; tile += ncl) {
             const TileCoord tc = decode_pair_tile<TT_MAX>(cum, gm, p.G, tile);
-            if (!wait_bounded(bar_acce + 8 * acc, aph ^ 1u, abort_flag, p.err,
-                                      p.timeout_ns)) {
-                ok = false;
-                break;
-            }
+            ok = __all_sync(0xffffffffu, wait_bounded(bar_acce + 8 * acc, aph ^ 1u, abort_flag,
+                                                      p.err, p.timeout_ns));
+            if (!ok) break;
             const uint32_t idesc = idesc_mxf4nvf4_pair((uint32_t)tc.w);
             const uint32_t d_tmem = tmem + acc * TT_MAX;
-            for (int ks = 0; ks < p.KS; ++ks, ++cnt) {
-                if (!wait_bounded(bar_full + 8 * s, ph, abort_flag, p.err, p.timeout_ns) ||
-                    !wait_bounded(bar_pfull + 8 * s, ph, abort_flag, p.err, p.timeout_ns) ||
-                    !wait_bounded(bar_sfready + 8 * s, ph, abort_flag, p.err, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
+            for (int ks = 0; ks < p.KS; ++ks) {
+                // both CTAs' tiles landed and all eight scale warps stored
+                ok = __all_sync(0xffffffffu, wait_bounded(bar_sfready + 8 * s, ph, abort_flag,
+                                                          p.err, p.timeout_ns));
+                if (!ok) break;
                 tc_fence_after();
-                const uint32_t sfw = tmem_sf + (uint32_t)(cnt % Cfg::SF_BUFS) * Cfg::SF_COLS;
+                const uint32_t sfw = tmem_sf + r * Cfg::SF_COLS;
                 const uint32_t sft = sfw + Cfg::SFW_COLS;
                 const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_W + s * Cfg::W_TILE);
                 const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_T + s * Cfg::T_TILE);
                 const uint32_t acc_in = ks != 0;
-                umma_pair_mxf4nvf4(d_tmem, ad, bd, idesc, sfw, sft, acc_in);
-                umma_pair_mxf4nvf4(d_tmem, ad + 2, bd + 2, idesc, sfw + 4, sft + 4 * Cfg::NA, 1u);
-                umma_pair_mxf4nvf4(d_tmem, ad + 4, bd + 4, idesc, sfw + 8, sft + 8 * Cfg::NA, 1u);
-                umma_pair_mxf4nvf4(d_tmem, ad + 6, bd + 6, idesc, sfw + 12, sft + 12 * Cfg::NA, 1u);
-                umma_commit_pair_multicast(bar_empty + 8 * s, 0x3);
-                if (ks == p.KS - 1) umma_commit_pair_multicast(bar_accf + 8 * acc, 0x3);
+                if (elect_one()) {
+                    umma_pair_mxf4nvf4(d_tmem, ad, bd, idesc, sfw, sft, acc_in);
+                    umma_pair_mxf4nvf4(d_tmem, ad + 2, bd + 2, idesc, sfw + 4, sft + 4 * Cfg::NA, 1u);
+                    umma_pair_mxf4nvf4(d_tmem, ad + 4, bd + 4, idesc, sfw + 8, sft + 8 * Cfg::NA, 1u);
+                    umma_pair_mxf4nvf4(d_tmem, ad + 6, bd + 6, idesc, sfw + 12, sft + 12 * Cfg::NA, 1u);
+                    umma_commit_pair_multicast(bar_empty + 8 * s, 0x3);
+                    if (ks == p.KS - 1) umma_commit_pair_multicast(bar_accf + 8 * acc, 0x3);
+                }
+                __syncwarp();
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
+                if (++r == Cfg::SF_BUFS) r = 0;
             }
             if (++acc == Cfg::ACC_BUFS) { acc = 0; aph ^= 1u; }
         }
-        umma_commit_pair(bar_done);
+        if (elect_one()) umma_commit_pair(bar_done);
+        __syncwarp();
         volatile int no_abort = 0;
         wait_bounded(bar_done, 0, &no_abort, p.err, p.timeout_ns);
-    } else if (warp == 1 && lane == 0) {
-        // ------------------------------------------ tile relay (peer CTA)
-        const uint32_t r_pfull = mapa_shared(bar_pfull, 0);
+    } else if (warp == 3 || warp == 4 || warp == 9 || warp == 10) {
+        // ------------------------------- scale warps (one per TMEM lane quarter)
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t sfready_target = leader ? bar_sfready : mapa_shared(bar_sfready, 0);
         int s = 0;
         uint32_t ph = 0;
-        bool ok = true;
-        for (int tile = cid; tile < total && ok; tile += ncl) {
-            for (int ks = 0; ks < p.KS; ++ks) {
-                if (!wait_bounded(bar_full + 8 * s, ph, abort_flag, p.err, p.timeout_ns)) {
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_remote_relaxed(r_pfull + 8 * s);
-                if (++s == STAGES) { s = 0; ph ^= 1u; }
-            }
-        }
-    } else if (warp >= 3 && warp <= 6) {
-        // ------------------------------------------------ scale warps (MMA q)
-        const int q = warp - 3;
-        const uint32_t r_psf = mapa_shared(bar_psf, 0);
-        int s = 0;
-        uint32_t ph = 0;
+        int r = 0;
         long long cnt = 0;
         bool ok = true;
         for (int tile = cid; tile < total && ok; tile += ncl) {
-            for (int ks = 0; ks < p.KS; ++ks, ++cnt) {
-                ok = __all_sync(0xffffffffu, wait_bounded(bar_sfull + 8 * s, ph, abort_flag, p.err,
-                                                          p.timeout_ns));
+            for (int ks = 0; ks < p.KS; ++ks) {
+                ok = __all_sync(0xffffffffu, wait_bounded(bar_sfull + 8 * s, ph, abort_flag,
+                                                          p.err, p.timeout_ns));
                 if (!ok) break;
-                // atoms of MMA q: row i = tokens i, i+32, i+64, i+96 (+128a), word q
-                const uint8_t* plain = sbase + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN;
-                uint8_t* atoms = sbase + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS;
+                if (Cfg::SF_BUFS < STAGES && cnt >= Cfg::SF_BUFS) {
+                    // the MMAs of the stage that last used region r are done
+                    // (the leader's commit reaches both CTAs' empty barriers)
+                    const long long prev = cnt - Cfg::SF_BUFS;
+                    ok = __all_sync(0xffffffffu,
+                                    wait_bounded(bar_empty + 8 * (int)(prev % STAGES),
+                                                 (uint32_t)((prev / STAGES) & 1), abort_flag,
+                                                 p.err, p.timeout_ns));
+                    if (!ok) break;
+                }
+                tc_fence_after();
+                // weights (this CTA's 128 rows): column 4q + c = word c of row
+                // `lane` of atom q
+                const uint8_t* wsf = sbase + Cfg::OFF_WSF + s * Cfg::WSF_STAGE + lane * 16;
+                uint32_t w[16];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(wsf + 512 * q);
+                    w[4 * q] = v.x;
+                    w[4 * q + 1] = v.y;
+                    w[4 * q + 2] = v.z;
+                    w[4 * q + 3] = v.w;
+                }
+                // tokens (all w rows): column 4(q NA + a) + c = word q of plain
+                // row 128a + 32c + lane
+                const uint8_t* plain = sbase + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN + lane * 16;
+                uint32_t t[16 * Cfg::NA];
 #pragma unroll
                 for (int a = 0; a < Cfg::NA; ++a) {
-                    uint32_t wv[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
-                    for (int j = 0; j < Cfg::JMAX; ++j)
-                        if (128 * a + 32 * j < TT_MAX)
-                            wv[j] = word_of(*reinterpret_cast<const uint4*>(plain + (128 * a + 32 * j + lane) * 16), q);
-                    *reinterpret_cast<uint4*>(atoms + (q * Cfg::NA + a) * 512 + lane * 16) =
-                        make_uint4(wv[0], wv[1], wv[2], wv[3]);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (!leader) {
-                        mbar_arrive_remote_relaxed(r_psf + 8 * s);
-                    } else {
-                        ok = wait_bounded(bar_psf + 8 * s, ph, abort_flag, p.err, p.timeout_ns);
-                        if (ok && cnt >= Cfg::SF_BUFS) {
-                            // the MMAs that last read this scale region are done
-                            const long long prev = cnt - Cfg::SF_BUFS;
-                            ok = wait_bounded(bar_empty + 8 * (int)(prev % STAGES),
-                                                      (uint32_t)((prev / STAGES) & 1), abort_flag,
-                                                      p.err, p.timeout_ns);
-                        }
-                        if (ok) {
-                            tc_fence_after();
-                            const uint32_t sfw = tmem_sf + (uint32_t)(cnt % Cfg::SF_BUFS) * Cfg::SF_COLS;
-                            const uint32_t sft = sfw + Cfg::SFW_COLS;
-                            tmem_cp_pair_32x128b_x4(
-                                sfw + 4 * q, sdesc_rows16(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE + 512 * q));
-#pragma unroll
-                            for (int a = 0; a < Cfg::NA; ++a)
-                                tmem_cp_pair_32x128b_x4(
-                                    sft + 4 * (q * Cfg::NA + a),
-                                    sdesc_rows16(base + Cfg::OFF_TSFA + s * Cfg::TSF_ATOMS + (q * Cfg::NA + a) * 512));
-                            umma_commit_pair(bar_sfready + 8 * s);
-                        }
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (128 * a + 32 * c < TT_MAX)
+                            v = *reinterpret_cast<const uint4*>(plain + (128 * a + 32 * c) * 16);
+                        t[4 * (0 * Cfg::NA + a) + c] = v.x;
+                        t[4 * (1 * Cfg::NA + a) + c] = v.y;
+                        t[4 * (2 * Cfg::NA + a) + c] = v.z;
+                        t[4 * (3 * Cfg::NA + a) + c] = v.w;
                     }
                 }
-                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                const uint32_t sfw = tmem_sf + r * Cfg::SF_COLS + lane_off;
+                tmem_st_32x32b_x16(sfw, w);
+#pragma unroll
+                for (int h = 0; h < Cfg::NA; ++h)
+                    tmem_st_32x32b_x16(sfw + Cfg::SFW_COLS + 16 * h, t + 16 * h);
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (warp == 3) {   // this CTA's operand tiles landed, too
+                    ok = __all_sync(0xffffffffu, wait_bounded(bar_full + 8 * s, ph, abort_flag,
+                                                              p.err, p.timeout_ns));
+                    if (!ok) break;
+                }
+                if (lane == 0) {
+                    if (leader) mbar_arrive(sfready_target + 8 * s);
+                    else mbar_arrive_remote_relaxed(sfready_target + 8 * s);
+                }
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
+                if (++r == Cfg::SF_BUFS) r = 0;
+                ++cnt;
             }
         }
-        if (lane == 0 && leader) {
-            umma_commit_pair(bar_done_sc + 8 * q);
-            volatile int no_abort = 0;
-            wait_bounded(bar_done_sc + 8 * q, 0, &no_abort, p.err, p.timeout_ns);
-        }
-    } else if (warp >= 7) {
+    } else if (warp >= 5 && warp <= 8) {
         // ------------------------------------------------------------ epilogue
-        const int ew = warp - 7;
+        const int ew = warp - 5;
         const int quad = warp & 3;
         uint8_t* stage_buf = sbase + Cfg::OFF_EPI + ew * (16 * 32 * 2);
         const uint32_t acce_target = leader ? bar_acce : mapa_shared(bar_acce, 0);
@@ -392,7 +377,7 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
         for (int tile = cid; tile < total; tile += ncl) {
             const TileCoord tc = decode_pair_tile<TT_MAX>(cum, gm, p.G, tile);
             const bool ok = __all_sync(0xffffffffu, wait_bounded(bar_accf + 8 * acc, aph,
-                                                                         abort_flag, p.err, p.timeout_ns));
+                                                                 abort_flag, p.err, p.timeout_ns));
             if (!ok) break;
             tc_fence_after();
             const float al = __ldg(p.alpha + tc.g);
@@ -404,12 +389,12 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
 #pragma unroll 1
             for (int c = 0; c < TT_MAX / 16; ++c) {
                 if (c * 16 >= tc.w) break;
-                uint32_t r[16];
-                tmem_ld_32x32b_x16(tbase + c * 16, r);
+                uint32_t rr[16];
+                tmem_ld_32x32b_x16(tbase + c * 16, rr);
                 tmem_wait_ld();
                 __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stage_buf);
 #pragma unroll
-                for (int t = 0; t < 16; ++t) sb[t * 32 + lane] = __float2bfloat16_rn(al * __uint_as_float(r[t]));
+                for (int t = 0; t < 16; ++t) sb[t * 32 + lane] = __float2bfloat16_rn(al * __uint_as_float(rr[t]));
                 __syncwarp();
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
@@ -433,7 +418,7 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
 
     tc_fence_before();
     __syncthreads();
-    cluster_sync_all();   // the leader's MMAs and copies are drained in both CTAs
+    cluster_sync_all();   // the leader's MMAs are drained; no remote arrive is in flight
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem, Cfg::TMEM_COLS);

@@ -32,7 +32,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 int g_sm_cap = 0;
-bool g_pair_enabled = false;   // CTA-pair prefill kernel: opt-in (see nvfp4gg.h)
+int g_pair_mode = 2;   // CTA-pair prefill kernel: 0 off, 1 on, 2 automatic (see nvfp4gg.h)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 unsigned long long g_timeout_ns = 2000000000ull;   // 2 s per device-side wait
 
@@ -89,7 +89,7 @@ int encode_u8_3d(CUtensorMap* m, const void* ptr, uint64_t d0, uint64_t d1, uint
 }
 
 // Token tensor maps, one per tile width 16, 32, ..., tt_max (widths a call
-// can use: at most M_max rounded up to 16; the others repeat the 16-row map).
+// can use: at most M_max rounded up to 32; the others repeat the 16-row map).
 // Encoding costs microseconds per map, so the last few sets are cached by
 // (A, A_sf, G, M_max, K, tt_max).
 struct TokenMaps {
@@ -121,7 +121,9 @@ int token_maps(const void* A, const void* A_sf, int G, int M_max, int K, int tt_
     g_maps_next = (g_maps_next + 1) % kMapCache;
     m.A = nullptr;   // invalid until fully encoded
     const uint64_t kb = (uint64_t)K / 2, ks = (uint64_t)K / 16;
-    const int rows_cap = ((M_max + 15) / 16) * 16;
+    // widths a call can use: M_max rounded up to 16 (single-CTA tiles) or to
+    // 32 (CTA-pair tiles); rows past M_max read as zero
+    const int rows_cap = ((M_max + 31) / 32) * 32;
     int rc = NVFP4GG_OK;
     for (int i = 0; i < kMaxWidths; ++i) {
         const uint32_t rows = 16u * (i + 1);
@@ -208,8 +210,12 @@ int launch_pair_variant(DeviceState* d, int slot, const GemmParams& p, cudaStrea
 constexpr int kNarrowTT = 32, kNarrowStages = 8;
 constexpr int kWideTT = 192, kWideStages = 4;
 // Larger experts with N a multiple of 256: CTA pairs (M = 256 per MMA),
-// token tiles of up to 160 split 80 + 80 rows, six ring stages.
-constexpr int kPairTT = 160, kPairStages = 6;
+// token tiles of up to 192 split 96 + 96 rows, six ring stages.
+constexpr int kPairTT = 192, kPairStages = 6;
+// Automatic pair mode: CTA pairs for prefill calls up to this M_max (a few
+// token tiles per expert: the weight stream dominates and the pair's halved
+// token staging and deeper ring pay); compute-heavy experts stay single.
+constexpr int kPairAutoMaxRows = 256;
 
 }  // namespace
 
@@ -302,7 +308,8 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
     if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
 
     const bool narrow = M_max <= 64;
-    const bool pair = !narrow && N % 256 == 0 && g_pair_enabled;
+    const bool pair = !narrow && N % 256 == 0 &&
+                      (g_pair_mode == 1 || (g_pair_mode == 2 && M_max <= kPairAutoMaxRows));
     const int tt_max = narrow ? kNarrowTT : pair ? kPairTT : kWideTT;
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
@@ -476,10 +483,10 @@ int nvfp4_gg_set_sm_count(int sm_count) {
     return NVFP4GG_OK;
 }
 
-int nvfp4_gg_set_pair_mode(int enable) {
-    if (enable != 0 && enable != 1) return NVFP4GG_ERR_SHAPE;
+int nvfp4_gg_set_pair_mode(int mode) {
+    if (mode < 0 || mode > 2) return NVFP4GG_ERR_SHAPE;
     std::lock_guard<std::mutex> lock(g_mu);
-    g_pair_enabled = enable != 0;
+    g_pair_mode = mode;
     return NVFP4GG_OK;
 }
 

@@ -147,9 +147,11 @@ def test_noalloc_splitk_argument_checks(lib):
 def test_sm_cap_and_watchdog_argument_checks(lib):
     assert lib.nvfp4_gg_set_sm_count(-1) == binding.ERR_SHAPE
     assert lib.nvfp4_gg_set_sm_count(0) == binding.OK
-    assert lib.nvfp4_gg_set_pair_mode(2) == binding.ERR_SHAPE
+    assert lib.nvfp4_gg_set_pair_mode(3) == binding.ERR_SHAPE
+    assert lib.nvfp4_gg_set_pair_mode(-1) == binding.ERR_SHAPE
     assert lib.nvfp4_gg_set_pair_mode(1) == binding.OK
     assert lib.nvfp4_gg_set_pair_mode(0) == binding.OK
+    assert lib.nvfp4_gg_set_pair_mode(2) == binding.OK   # the default: automatic
     assert lib.nvfp4_gg_selftest_watchdog(10, None) == binding.ERR_SHAPE
     assert lib.nvfp4_gg_selftest_watchdog(10 ** 11, None) == binding.ERR_SHAPE
 

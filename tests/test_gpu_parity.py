@@ -114,8 +114,9 @@ def test_c1_poisoned_rows_ignored(lib):
     (2, 64, 256, 1024, [64, 31]),                           # narrow kernel, M_max = 64
     (4, 200, 272, 768, [200, 129, 128, 1]),                 # wide kernel, ragged widths
     (2, 256, 384, 512, [256, 255]),                         # wide kernel, 2 x 128 tiles
-    (2, 192, 256, 2048, [192, 177]),                        # wide kernel, full 192-row tile,
-                                                            # 8 stages over 2 scale regions
+    (2, 192, 384, 2048, [192, 177]),                        # wide single-CTA kernel (N % 256
+                                                            # != 0), full 192-row tile, 8 stages
+                                                            # over 2 scale regions
     (1, 1, 16, 256, [1]),                                   # minimum sizes
     (6, 24, 128, 256, [0, 0, 0, 0, 0, 0]),                  # every expert empty
 ])
@@ -136,7 +137,7 @@ def test_prefill_variants_pair_and_single(lib, G, M_max, N, K, masked, pair):
     try:
         check_full(d, run_gpu(d))
     finally:
-        lib.nvfp4_gg_set_pair_mode(False)
+        lib.nvfp4_gg_set_pair_mode(lib.PAIR_AUTO)
 
 
 @pytest.mark.parametrize("key", ["c4", "c5"])
@@ -146,7 +147,7 @@ def test_full_size_sampled_pair_kernel(lib, key):
         d = W.generate(W.CONFIGS[key])
         check_sampled(d, run_gpu(d), rows_per_group=3, cols=48)
     finally:
-        lib.nvfp4_gg_set_pair_mode(False)
+        lib.nvfp4_gg_set_pair_mode(lib.PAIR_AUTO)
 
 
 def run_gpu_splitk(d, split_k):
