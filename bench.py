@@ -248,6 +248,8 @@ def main():
     ap.add_argument("--config", default="c2", choices=sorted(W.CONFIGS) + sorted(W.EXTRA))
     ap.add_argument("--splitk", type=int, default=-1,
                     help="time nvfp4_grouped_gemm_nt_masked_splitk with this split (0 = automatic)")
+    ap.add_argument("--swiglu", action="store_true",
+                    help="time the fused GEMM1 + SwiGLU entry point (output N/2 columns)")
     ap.add_argument("--pair-mode", default="auto", choices=["auto", "on", "off"],
                     help="prefill kernel family: CTA pairs (on), single CTAs (off), or the "
                          "library's automatic choice")
@@ -277,6 +279,9 @@ def main():
 
     d = W.generate(cfg)
     counts = W.algorithmic_counts(cfg, d["masked_m"])
+    if args.swiglu:   # the fused epilogue writes N/2 bf16 columns per valid row
+        counts["bytes"] -= counts["out_bytes"] // 2
+        counts["out_bytes"] //= 2
     stream = torch.cuda.current_stream()
 
     # one-time weight re-layout, timed separately (median of 5)
@@ -286,8 +291,9 @@ def main():
     for _ in range(5):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        binding.nvfp4_prepare_weights(prob.raw_B, prob.raw_Bsf, cfg.G, cfg.N, cfg.K, prob.B_prep,
-                                      prob.B_sf_prep)
+        prepare = (binding.nvfp4_prepare_weights_swiglu if args.swiglu
+                   else binding.nvfp4_prepare_weights)
+        prepare(prob.raw_B, prob.raw_Bsf, cfg.G, cfg.N, cfg.K, prob.B_prep, prob.B_sf_prep)
         e1.record()
         e1.synchronize()
         prep_ms.append(e0.elapsed_time(e1))
@@ -303,6 +309,13 @@ def main():
             binding.nvfp4_grouped_gemm_nt_masked_splitk(
                 prob.A, prob.A_sf, prob.B_prep, prob.B_sf_prep, prob.alpha, prob.masked_m, prob.C,
                 cfg.G, cfg.M_max, cfg.N, cfg.K, args.splitk, splitk_ws, splitk_bytes)
+    elif args.swiglu:
+        C_half = torch.empty((cfg.G, cfg.M_max, cfg.N // 2), dtype=torch.int16, device="cuda")
+
+        def run_step():
+            binding.nvfp4_grouped_gemm_nt_masked_swiglu(
+                prob.A, prob.A_sf, prob.B_prep, prob.B_sf_prep, prob.alpha, prob.masked_m, C_half,
+                cfg.G, cfg.M_max, cfg.N, cfg.K)
     else:
         run_step = prob.run
     for i in range(args.warmup):
@@ -381,7 +394,8 @@ def main():
         "prepare_weights_ms": statistics.median(prep_ms),
         "gpu_launches": args.steps,
         "entry_point": ("nvfp4_grouped_gemm_nt_masked_splitk(split_k=%d)" % args.splitk
-                        if args.splitk >= 0 else "nvfp4_grouped_gemm_nt_masked"),
+                        if args.splitk >= 0 else "nvfp4_grouped_gemm_nt_masked_swiglu"
+                        if args.swiglu else "nvfp4_grouped_gemm_nt_masked"),
         "pair_mode": args.pair_mode,
         "wall_s_timed_region": wall,
         "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
@@ -403,7 +417,9 @@ def main():
     line["e2e"] = {"value": counts["flops"] / (e2e_med / 1e3) / 1e12, "unit": UNIT,
                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                    "ms_per_step": e2e_med, "steps": args.e2e_steps,
-                   "how": "nvfp4_grouped_gemm_nt_masked_host on pinned host buffers: A and A_sf "
+                   "how": ("(plain GEMM: the host-buffer entry point has no SwiGLU variant) "
+                           if args.swiglu else "") +
+                          "nvfp4_grouped_gemm_nt_masked_host on pinned host buffers: A and A_sf "
                           "copied to the device, alpha and masked_m read and the valid rows of C "
                           "written by the kernel in host memory, stream sync; wall clock per "
                           "step (Python call included)"}

@@ -177,6 +177,30 @@ int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(const void* A, const void* A_sf,
                                                 int N, int K, int split_k, void* stream);
 
 /*
+ * GEMM1 of an MoE expert block with its SwiGLU activation fused into the
+ * epilogue: the step that follows this GEMM on the page "LLM-Assisted Kernel
+ * Development in CuTe DSL, Gluon, Helion and Triton" (mixture-of-experts
+ * section: per expert GEMM1 -> SwiGLU -> GEMM2, I = 2048).  B is GEMM1's
+ * weight [G][N][K] with N = 2 I: rows 0 .. I-1 the gate projection, rows
+ * I .. 2I-1 the up projection (the page does not fix the order; this is the
+ * reading taken).  For m < masked_m[g] and j < I:
+ *     h(row)     = alpha[g] * sum_k A[g][m][k] * B[g][row][k]   (fp32 accumulation)
+ *     C[g][m][j] = bf16( silu(h(j)) * h(I + j) ),   silu(x) = x / (1 + e^-x)
+ * C is bf16 [G][M_max][N/2], row-major; rows m >= masked_m[g] are never
+ * written.  B and B_sf must come from nvfp4_prepare_weights_swiglu (same
+ * sizes as nvfp4_prepare_weights), which interleaves gate and up rows so that
+ * one weight tile holds both halves of the outputs it produces.  N % 128 == 0
+ * (NVFP4GG_ERR_SHAPE otherwise); other arguments and limits as in
+ * nvfp4_grouped_gemm_nt_masked.  Runs on the single-CTA kernels (no CTA
+ * pairs, no split-K).
+ */
+int nvfp4_prepare_weights_swiglu(const void* B, const void* B_sf, int G, int N, int K,
+                                 void* B_prep, void* B_sf_prep, void* stream);
+int nvfp4_grouped_gemm_nt_masked_swiglu(const void* A, const void* A_sf, const void* B,
+                                        const void* B_sf, const float* alpha, const int* masked_m,
+                                        void* C, int G, int M_max, int N, int K, void* stream);
+
+/*
  * End-to-end variant for callers whose activations live in host memory.
  *   h_A, h_A_sf, h_alpha, h_masked_m: HOST buffers laid out as above (pinned
  *       memory gives asynchronous copies)

@@ -33,6 +33,8 @@ EXPORTS = (
     "nvfp4_splitk_workspace_bytes",
     "nvfp4_grouped_gemm_nt_masked_splitk",
     "nvfp4_grouped_gemm_nt_masked_splitk_noalloc",
+    "nvfp4_prepare_weights_swiglu",
+    "nvfp4_grouped_gemm_nt_masked_swiglu",
     "nvfp4_host_staging_bytes",
     "nvfp4_grouped_gemm_nt_masked_host",
     "nvfp4_gg_set_sm_count",
@@ -77,6 +79,10 @@ def load():
     lib.nvfp4_grouped_gemm_nt_masked_splitk.restype = i
     lib.nvfp4_grouped_gemm_nt_masked_splitk_noalloc.argtypes = [vp] * 7 + [i] * 5 + [vp]
     lib.nvfp4_grouped_gemm_nt_masked_splitk_noalloc.restype = i
+    lib.nvfp4_prepare_weights_swiglu.argtypes = [vp, vp, i, i, i, vp, vp, vp]
+    lib.nvfp4_prepare_weights_swiglu.restype = i
+    lib.nvfp4_grouped_gemm_nt_masked_swiglu.argtypes = [vp] * 7 + [i] * 4 + [vp]
+    lib.nvfp4_grouped_gemm_nt_masked_swiglu.restype = i
     lib.nvfp4_host_staging_bytes.argtypes = [i] * 4
     lib.nvfp4_host_staging_bytes.restype = sz
     lib.nvfp4_grouped_gemm_nt_masked_host.argtypes = [vp] * 7 + [i] * 4 + [vp, sz, vp]
@@ -156,6 +162,20 @@ def nvfp4_grouped_gemm_nt_masked(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max,
                                                _ptr(alpha), _ptr(masked_m), _ptr(C),
                                                G, M_max, N, K, _stream(stream)),
            "nvfp4_grouped_gemm_nt_masked")
+
+
+def nvfp4_prepare_weights_swiglu(B, B_sf, G, N, K, B_prep, B_sf_prep, stream=None):
+    _check(load().nvfp4_prepare_weights_swiglu(_ptr(B), _ptr(B_sf), G, N, K, _ptr(B_prep),
+                                               _ptr(B_sf_prep), _stream(stream)),
+           "nvfp4_prepare_weights_swiglu")
+
+
+def nvfp4_grouped_gemm_nt_masked_swiglu(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K,
+                                        stream=None):
+    _check(load().nvfp4_grouped_gemm_nt_masked_swiglu(_ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf),
+                                                      _ptr(alpha), _ptr(masked_m), _ptr(C),
+                                                      G, M_max, N, K, _stream(stream)),
+           "nvfp4_grouped_gemm_nt_masked_swiglu")
 
 
 def nvfp4_splitk_workspace_bytes(G, M_max, N, K, split_k=0) -> int:

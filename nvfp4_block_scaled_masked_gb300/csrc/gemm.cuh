@@ -194,7 +194,13 @@ __device__ __forceinline__ TileCoord decode_tile(const int* cum, const int* gm, 
     return c;
 }
 
-template <int TT_MAX, int STAGES>
+// SWIGLU: the fused GEMM1 epilogue.  The weights are prepared with gate and
+// up rows interleaved (nvfp4_prepare_weights_swiglu): in each 32-row lane
+// quarter of a 128-row block, rows 0..15 are gate rows and rows 16..31 the
+// up rows of the same 16 output columns.  Lane l < 16 then combines its
+// h_gate = alpha * acc with lane l + 16's h_up into silu(h_gate) * h_up, and
+// C is bf16 [G][M_max][N/2], output column = 64 * block + 16 * quarter + l.
+template <int TT_MAX, int STAGES, bool SWIGLU = false>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
     using Cfg = KCfg<TT_MAX, STAGES>;
@@ -498,7 +504,36 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             const int tr = lane >> 2, tq = lane & 3;
             const bool n_ok = n0 + 8 * tq < p.N;
             __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stage_buf);
-            if (p.split == 1) {
+            if (SWIGLU) {
+                // output columns oc0 .. oc0 + 15 of this warp; a stage of
+                // [16 tokens][16 columns] bf16, stored by 32 lanes x 16 bytes
+                const int NO = p.N >> 1;
+                const int oc0 = tc.nt * 64 + quad * 16;
+#pragma unroll 1
+                for (int c = 0; c < TT_MAX / 16; ++c) {
+                    if (c * 16 >= tc.w) break;
+                    uint32_t r[16];
+                    tmem_ld_32x32b_x16(tbase + c * 16, r);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) {
+                        const float h = al * __uint_as_float(r[t]);
+                        const float up = __shfl_xor_sync(0xffffffffu, h, 16);
+                        const float y = h / (1.0f + __expf(-h)) * up;   // lanes < 16: silu(gate) * up
+                        if (lane < 16) sb[t * 16 + lane] = __float2bfloat16_rn(y);
+                    }
+                    __syncwarp();
+                    const int t = lane >> 1, hh = lane & 1;
+                    const int tok = tc.t0 + c * 16 + t;
+                    const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + t * 32 + hh * 16);
+                    if (tok < t_end && oc0 < NO)
+                        *reinterpret_cast<uint4*>(p.C + ((size_t)tc.g * p.M_max + tok) * NO + oc0 + 8 * hh) = v;
+                    __syncwarp();
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_acce + 8 * acc);
+            } else if (p.split == 1) {
 #pragma unroll 1
                 for (int c = 0; c < TT_MAX / 16; ++c) {
                     if (c * 16 >= tc.w) break;
@@ -674,8 +709,20 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int n, int*
 // Weight-scale re-layout: B_sf u8 [G][N][K/16] -> atoms [G][NT][K/64][32][4][4]
 // where atom byte (i, j, b) is the scale of row 128*nt + 32*j + i, K block
 // 4*kc + b (zero for rows >= N).  One thread per 16-byte atom row.
+// Source row of prepared weight row n: the identity, or with `swiglu` the
+// gate/up interleave the fused SwiGLU epilogue reads (N % 128 == 0): in
+// 128-row block b, lane quarter q, row l of 32 holds gate row
+// 64b + 16q + l (l < 16) or up row N/2 + 64b + 16q + (l - 16).
+__device__ __forceinline__ int prepared_source_row(int n, int N, int swiglu) {
+    if (!swiglu) return n;
+    const int b = n >> 7, q = (n >> 5) & 3, l = n & 31;
+    const int col = 64 * b + 16 * q + (l & 15);
+    return l < 16 ? col : (N >> 1) + col;
+}
+
 __global__ void relayout_weight_scales_kernel(const uint8_t* __restrict__ bsf,
-                                              uint8_t* __restrict__ out, int G, int N, int K) {
+                                              uint8_t* __restrict__ out, int G, int N, int K,
+                                              int swiglu) {
     const int NT = (N + 127) / 128;
     const int KC = K / 64;
     const long long rows = (long long)G * NT * KC * 32;
@@ -692,7 +739,8 @@ __global__ void relayout_weight_scales_kernel(const uint8_t* __restrict__ bsf,
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int n = nt * 128 + 32 * j + i;
-            wv[j] = n < N ? *reinterpret_cast<const uint32_t*>(bsf + ((size_t)g * N + n) * ks16 + 4 * kc)
+            wv[j] = n < N ? *reinterpret_cast<const uint32_t*>(
+                                bsf + ((size_t)g * N + prepared_source_row(n, N, swiglu)) * ks16 + 4 * kc)
                           : 0u;
         }
         *reinterpret_cast<uint4*>(out + idx * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
@@ -705,7 +753,8 @@ __global__ void relayout_weight_scales_kernel(const uint8_t* __restrict__ bsf,
 // (16-byte chunk c of row r at chunk c ^ (r % 8)), zero for rows >= N.  One
 // thread per 16-byte chunk.
 __global__ void relayout_weight_codes_kernel(const uint8_t* __restrict__ b,
-                                             uint8_t* __restrict__ out, int G, int N, int K) {
+                                             uint8_t* __restrict__ out, int G, int N, int K,
+                                             int swiglu) {
     const int NT = (N + 127) / 128;
     const int KS = K / 256;
     const long long chunks = (long long)G * NT * KS * 1024;
@@ -722,7 +771,8 @@ __global__ void relayout_weight_codes_kernel(const uint8_t* __restrict__ b,
         const int n = nt * 128 + r;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (n < N)
-            v = *reinterpret_cast<const uint4*>(b + ((size_t)g * N + n) * row_bytes + (size_t)ks * 128 + c * 16);
+            v = *reinterpret_cast<const uint4*>(b + ((size_t)g * N + prepared_source_row(n, N, swiglu)) * row_bytes +
+                                                (size_t)ks * 128 + c * 16);
         *reinterpret_cast<uint4*>(out + (idx >> 3) * 128 + ((c ^ (r & 7)) * 16)) = v;
     }
 }

@@ -157,10 +157,10 @@ int check_gemm_shape(int G, int M_max, int N, int K) {
     return NVFP4GG_OK;
 }
 
-template <int TT, int ST>
+template <int TT, int ST, bool SWIGLU = false>
 int launch_variant(DeviceState* d, int slot, const GemmParams& p, cudaStream_t stream) {
     using Cfg = KCfg<TT, ST>;
-    auto kern = gemm_nt_masked_kernel<TT, ST>;
+    auto kern = gemm_nt_masked_kernel<TT, ST, SWIGLU>;
     if (!d->attr_set[slot]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::SMEM_BYTES) != cudaSuccess)
@@ -247,8 +247,13 @@ int nvfp4_prepared_weight_bytes(int G, int N, int K, size_t* b_bytes, size_t* sf
     return NVFP4GG_OK;
 }
 
-int nvfp4_prepare_weights(const void* B, const void* B_sf, int G, int N, int K, void* B_prep,
-                          void* B_sf_prep, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Weight re-layout; `swiglu` interleaves gate and up rows (N % 128 == 0).
+int prepare_weights(const void* B, const void* B_sf, int G, int N, int K, void* B_prep,
+                    void* B_sf_prep, void* stream, int swiglu) {
     if (!B || !B_sf || !B_prep || !B_sf_prep) return NVFP4GG_ERR_NULL;
     size_t bb = 0, sb = 0;
     int rc = nvfp4_prepared_weight_bytes(G, N, K, &bb, &sb);
@@ -263,12 +268,27 @@ int nvfp4_prepare_weights(const void* B, const void* B_sf, int G, int N, int K, 
     const long long cap = 16LL * d->sms;
     long long blocks = ((long long)(bb / 16) + threads - 1) / threads;
     relayout_weight_codes_kernel<<<(int)(blocks < cap ? blocks : cap), threads, 0, st>>>(
-        static_cast<const uint8_t*>(B), static_cast<uint8_t*>(B_prep), G, N, K);
+        static_cast<const uint8_t*>(B), static_cast<uint8_t*>(B_prep), G, N, K, swiglu);
     if (cudaGetLastError() != cudaSuccess) return NVFP4GG_ERR_CUDA;
     blocks = ((long long)(sb / 16) + threads - 1) / threads;
     relayout_weight_scales_kernel<<<(int)(blocks < cap ? blocks : cap), threads, 0, st>>>(
-        static_cast<const uint8_t*>(B_sf), static_cast<uint8_t*>(B_sf_prep), G, N, K);
+        static_cast<const uint8_t*>(B_sf), static_cast<uint8_t*>(B_sf_prep), G, N, K, swiglu);
     return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" {
+
+int nvfp4_prepare_weights(const void* B, const void* B_sf, int G, int N, int K, void* B_prep,
+                          void* B_sf_prep, void* stream) {
+    return prepare_weights(B, B_sf, G, N, K, B_prep, B_sf_prep, stream, 0);
+}
+
+int nvfp4_prepare_weights_swiglu(const void* B, const void* B_sf, int G, int N, int K,
+                                 void* B_prep, void* B_sf_prep, void* stream) {
+    if (N % 128 != 0) return NVFP4GG_ERR_SHAPE;
+    return prepare_weights(B, B_sf, G, N, K, B_prep, B_sf_prep, stream, 1);
 }
 
 }  // extern "C"
@@ -297,7 +317,7 @@ int auto_split(DeviceState* d, long long tiles, int K) {
 
 int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf, const float* alpha,
                 const int* masked_m, void* C, int G, int M_max, int N, int K, int split,
-                float* ws_part, int* ws_cnt, void* stream) {
+                float* ws_part, int* ws_cnt, void* stream, bool swiglu = false) {
     if (!A || !A_sf || !B || !B_sf || !alpha || !masked_m || !C) return NVFP4GG_ERR_NULL;
     int rc = check_gemm_shape(G, M_max, N, K);
     if (rc != NVFP4GG_OK) return rc;
@@ -308,7 +328,7 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
     if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
 
     const bool narrow = M_max <= 64;
-    const bool pair = !narrow && N % 256 == 0 &&
+    const bool pair = !narrow && !swiglu && N % 256 == 0 &&
                       (g_pair_mode == 1 || (g_pair_mode == 2 && M_max <= kPairAutoMaxRows));
     const int tt_max = narrow ? kNarrowTT : pair ? kPairTT : kWideTT;
     GemmParams p;
@@ -338,6 +358,9 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
         p.ws_part = ws_part;
         p.ws_cnt = ws_cnt;
     }
+    if (swiglu)
+        return narrow ? launch_variant<kNarrowTT, kNarrowStages, true>(d, 3, p, st)
+                      : launch_variant<kWideTT, kWideStages, true>(d, 4, p, st);
     if (narrow) return launch_variant<kNarrowTT, kNarrowStages>(d, 0, p, st);
     if (pair) return launch_pair_variant<kPairTT, kPairStages>(d, 2, p, st);
     return launch_variant<kWideTT, kWideStages>(d, 1, p, st);
@@ -352,6 +375,14 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
                                  int N, int K, void* stream) {
     return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr, nullptr,
                        stream);
+}
+
+int nvfp4_grouped_gemm_nt_masked_swiglu(const void* A, const void* A_sf, const void* B,
+                                        const void* B_sf, const float* alpha, const int* masked_m,
+                                        void* C, int G, int M_max, int N, int K, void* stream) {
+    if (N % 128 != 0) return NVFP4GG_ERR_SHAPE;
+    return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr, nullptr,
+                       stream, true);
 }
 
 size_t nvfp4_splitk_workspace_bytes(int G, int M_max, int N, int K, int split_k) {

@@ -10,6 +10,9 @@ Two implementations live here, written independently of each other:
   fp64, built with gcc (OpenMP over independent output rows only).
 * ``gemm_numpy`` is a second, NumPy fp64 restatement used to cross-check the
   C oracle on small shapes (table lookup, scale broadcast, ``einsum``).
+* ``swiglu`` applies the MoE block's SwiGLU step to GEMM1's unrounded fp64
+  output (``silu(gate) * up``, one bf16 rounding), for the fused GEMM1
+  epilogue.
 
 The operation is the one the page "The CuteDSL Gamble: Chasing Kernel
 Efficiency on Blackwell GPUs" describes for FlashInfer's
@@ -218,6 +221,53 @@ def bf16_bits_numpy(x) -> np.ndarray:
     if np.any(e >= 255):
         raise ValueError("bf16_bits_numpy: overflow")
     return out.astype(np.uint16)
+
+
+def bf16_bits_any(x) -> np.ndarray:
+    """fp64 -> bf16 bits, round to nearest even, over bf16's whole finite range:
+    the normal range as bf16_bits_numpy, below 2^-126 onto bf16's subnormal
+    grid (multiples of 2^-133, ties to even; 128 * 2^-133 is the smallest
+    normal)."""
+    x = np.asarray(x, dtype=np.float64)
+    out = np.zeros(x.shape, dtype=np.uint16)
+    tiny = np.abs(x) < 2.0 ** -126
+    if np.any(~tiny):
+        out[~tiny] = bf16_bits_numpy(x[~tiny])
+    if np.any(tiny):
+        k = np.rint(np.abs(x[tiny]) / 2.0 ** -133).astype(np.uint16)   # rint: ties to even
+        out[tiny] = (np.signbit(x[tiny]).astype(np.uint16) << np.uint16(15)) | k
+    return out
+
+
+def silu(x):
+    """silu(x) = x * sigmoid(x) = x / (1 + e^-x), fp64 (e^-x overflowing to
+    inf gives the limit 0)."""
+    x = np.asarray(x, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return x / (1.0 + np.exp(-x))
+
+
+def swiglu(ref64, masked_m, C_init_half):
+    """The SwiGLU step after GEMM1 in the MoE expert block of the page
+    "LLM-Assisted Kernel Development in CuTe DSL, Gluon, Helion and Triton"
+    (mixture-of-experts section: per expert GEMM1 -> SwiGLU -> GEMM2).  From
+    GEMM1's unrounded fp64 output ref64 [G, M_max, N] (N = 2I; reading: the
+    first I columns are the gate projection, the last I the up projection):
+    out[g, m, j] = silu(ref64[g, m, j]) * ref64[g, m, I + j] in fp64, rounded
+    once to bf16.  Returns (C bits uint16 [G, M_max, I], a copy of
+    C_init_half with rows m < masked_m[g] written; out64 with NaN elsewhere)."""
+    G, M_max, N = ref64.shape
+    I = N // 2
+    C = np.array(C_init_half, dtype=np.uint16, copy=True).reshape(G, M_max, I)
+    out = np.full((G, M_max, I), np.nan)
+    for g in range(G):
+        m = int(masked_m[g])
+        if m == 0:
+            continue
+        y = silu(ref64[g, :m, :I]) * ref64[g, :m, I:]
+        out[g, :m] = y
+        C[g, :m] = bf16_bits_any(y)
+    return C, out
 
 
 def tolerance_ok(gpu_vals, ref64, max_abs):

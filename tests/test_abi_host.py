@@ -158,3 +158,15 @@ def test_sm_cap_and_watchdog_argument_checks(lib):
 
 def test_library_targets_sm103a_only():
     assert build.ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_swiglu_argument_checks(lib):
+    f = lib.nvfp4_grouped_gemm_nt_masked_swiglu
+    args = [FAKE] * 7 + [2, 16, 256, 512, None]
+    a = list(args); a[9] = 192                    # N % 128 != 0
+    assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[0] = None
+    assert f(*a) == binding.ERR_NULL
+    p = lib.nvfp4_prepare_weights_swiglu
+    assert p(FAKE, FAKE, 2, 192, 512, FAKE + 4096, FAKE + 8192, None) == binding.ERR_SHAPE
+    assert p(None, FAKE, 2, 256, 512, FAKE + 4096, FAKE + 8192, None) == binding.ERR_NULL

@@ -330,3 +330,79 @@ def test_golden_tiny_case_regression():
     C, ref = oracle.gemm(A, A_sf, B, B_sf, alpha, mm, np.full((G, M, N), 0x7FC0, np.uint16),
                          G, M, N, K)
     np.testing.assert_array_equal(C.ravel(), np.array(gd["C_bits"], dtype=np.uint16))
+
+
+# ------------------------------------------------ SwiGLU step after GEMM1
+
+def test_silu_closed_forms():
+    """sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4 give silu(+-ln 3) in closed
+    form; silu(x) - silu(-x) = x for every x; the limits at +-infinity."""
+    ln3 = np.log(3.0)
+    assert oracle.silu(0.0) == 0.0
+    np.testing.assert_allclose(oracle.silu(ln3), 0.75 * ln3, rtol=4e-16)
+    np.testing.assert_allclose(oracle.silu(-ln3), -0.25 * ln3, rtol=4e-16)
+    x = np.random.default_rng(3).normal(0, 20, 1000)
+    np.testing.assert_allclose(oracle.silu(x) - oracle.silu(-x), x, rtol=1e-12, atol=1e-12)
+    assert oracle.silu(1000.0) == 1000.0
+    assert oracle.silu(-1000.0) == 0.0
+
+
+def _one_token_gemm1(gate_vals, up_vals):
+    """G=1, one token with the value 1 at k = 0 (scale 1.0); weight row j holds
+    its value at k = 0 (e2m1 code times an e4m3 scale), so h_j is that value."""
+    N, K = 2 * len(gate_vals), 16
+    enc = {1: (0x2, 0x38), 3: (0x5, 0x38), 6: (0x7, 0x38), 24: (0x7, 0x48), -24: (0xF, 0x48)}
+    A = np.zeros((1, 1, K // 2), np.uint8)
+    A[0, 0, 0] = 0x2
+    A_sf = np.full((1, 1, K // 16), 0x38, np.uint8)
+    B = np.zeros((1, N, K // 2), np.uint8)
+    B_sf = np.full((1, N, K // 16), 0x38, np.uint8)
+    for j, v in enumerate(list(gate_vals) + list(up_vals)):
+        B[0, j, 0], B_sf[0, j, 0] = enc[v]
+    mm = np.array([1], np.int32)
+    _, ref = oracle.gemm(A, A_sf, B, B_sf, np.ones(1, np.float32), mm,
+                         np.zeros((1, 1, N), np.uint16), 1, 1, N, K)
+    return ref, mm
+
+
+def test_swiglu_gate_is_the_first_half():
+    """h = [gate | up] = [24, -24 | 3, 6]: out = silu(24)*3 rounds to exactly 72
+    (the swapped reading would give silu(3)*24 = 68.6), and silu(-24)*6 is a
+    tiny negative number, not silu(6)*(-24) = -143.6."""
+    ref, mm = _one_token_gemm1([24, -24], [3, 6])
+    np.testing.assert_array_equal(ref[0, 0], [24.0, -24.0, 3.0, 6.0])
+    C, out = oracle.swiglu(ref, mm, np.zeros((1, 1, 2), np.uint16))
+    assert C[0, 0, 0] == 0x4290                    # bf16(72.0)
+    assert -1e-8 < out[0, 0, 1] < 0
+
+
+def test_swiglu_is_linear_in_up_and_not_in_gate():
+    """Doubling every up-row scale (e4m3 exponent + 1) doubles the output
+    exactly; doubling the gate-row scales does not."""
+    G, M, N, K = 2, 6, 64, 256
+    d = W.generate(W.custom(G, M, N, K, masked_m=[6, 3]), seed=21)
+    init = np.full((G, M, N // 2), 0x7FC0, np.uint16)
+
+    def run(B_sf):
+        _, ref = oracle.gemm(d["A"], d["A_sf"], d["B"], B_sf, d["alpha"], d["masked_m"],
+                             d["C_init"], G, M, N, K)
+        return oracle.swiglu(ref, d["masked_m"], init)
+
+    C0, y0 = run(d["B_sf"])
+    up2 = d["B_sf"].copy()
+    up2[:, N // 2:] += 8
+    C1, y1 = run(up2)
+    gate2 = d["B_sf"].copy()
+    gate2[:, :N // 2] += 8
+    _, y2 = run(gate2)
+    for g in range(G):
+        m = d["masked_m"][g]
+        np.testing.assert_array_equal(y1[g, :m], 2.0 * y0[g, :m])
+        assert not np.allclose(y2[g, :m], 2.0 * y0[g, :m])
+        assert np.all(C0[g, m:] == 0x7FC0) and np.all(C1[g, m:] == 0x7FC0)
+
+
+def test_bf16_bits_any_subnormal_grid():
+    vals = np.array([1.0, -2.0 ** -130, 1.5 * 2.0 ** -133, 2.5 * 2.0 ** -133, 128 * 2.0 ** -133, -0.0])
+    want = torch.from_numpy(vals.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
+    np.testing.assert_array_equal(oracle.bf16_bits_any(vals), want.astype(np.uint16))
