@@ -177,6 +177,29 @@ int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(const void* A, const void* A_sf,
                                                 int N, int K, int split_k, void* stream);
 
 /*
+ * The GEMM with per-expert completion signals: the dst_signals argument of
+ * grouped_gemm_nt_masked on "The CuteDSL Gamble: Chasing Kernel Efficiency
+ * on Blackwell GPUs" ("The Message"), whose behaviour the page does not
+ * describe (reading taken: a consumer may start on expert g as soon as its
+ * output is complete, without waiting for the whole call).
+ *   dst_signals  device i32 [G], owned by the caller.  Each call increments
+ *                dst_signals[g] by exactly 1 after every valid row of expert
+ *                g's C has been stored, a device-scope fence in between;
+ *                experts with masked_m[g] = 0 are signalled at kernel start.
+ *                A consumer that sees the new value must load C with
+ *                acquire ordering (or fence) before reading it.
+ * Other arguments as in nvfp4_grouped_gemm_nt_masked; runs on the single-CTA
+ * kernels.  The per-expert counters behind the signals are a static array of
+ * the library (NVFP4GG_MAX_GROUPS ints per device), cleared on `stream`
+ * before each call: calls of this entry point that overlap on one device
+ * race on them.
+ */
+int nvfp4_grouped_gemm_nt_masked_signals(const void* A, const void* A_sf, const void* B,
+                                         const void* B_sf, const float* alpha, const int* masked_m,
+                                         void* C, int G, int M_max, int N, int K, int* dst_signals,
+                                         void* stream);
+
+/*
  * GEMM1 of an MoE expert block with its SwiGLU activation fused into the
  * epilogue: the step that follows this GEMM on the page "LLM-Assisted Kernel
  * Development in CuTe DSL, Gluon, Helion and Triton" (mixture-of-experts

@@ -74,6 +74,11 @@ struct GemmParams {
     int split;
     float* ws_part;
     int* ws_cnt;
+    // per-expert completion signals (null: none): signals[g] is incremented
+    // once per call after all of expert g's valid rows of C are stored;
+    // sig_cnt[G] counts finished tile parts (zero at kernel start)
+    int* signals;
+    int* sig_cnt;
 };
 
 // K stages [kb, ke) of split range sp of S over KS stages (balanced).
@@ -166,6 +171,27 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
 struct TileCoord {
     int g, nt, t0, w, m;
 };
+
+template <int TT_MAX>
+__device__ __forceinline__ int token_tiles(int m);
+
+// After one epilogue warp stored its part of a tile of expert tc.g: count the
+// part; the last of the expert's 4 x (tiles) parts resets the count and
+// increments the expert's signal.  Each lane fences its own stores first.
+template <int TT_MAX>
+__device__ __forceinline__ void signal_tile_part(const GemmParams& p, const TileCoord& tc, int lane) {
+    if (!p.signals) return;
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) {
+        const int parts = 4 * token_tiles<TT_MAX>(tc.m) * p.NT;
+        if (atomicAdd(p.sig_cnt + tc.g, 1) == parts - 1) {
+            p.sig_cnt[tc.g] = 0;
+            __threadfence();
+            atomicAdd(p.signals + tc.g, 1);
+        }
+    }
+}
 
 // Token tiles of an expert with m valid rows: ntt = ceil(m / TT_MAX) tiles of
 // equal width w = ceil(m / ntt) rounded up to 16 (the MMA's N granularity).
@@ -260,6 +286,8 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             m = m < 0 ? 0 : p.M_max;
         }
         gm[g] = m;
+        // an expert without valid rows is complete from the start
+        if (p.signals && m == 0 && blockIdx.x == 0) atomicAdd(p.signals + g, 1);
     }
     __syncthreads();
     if (warp == 0) {
@@ -533,6 +561,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_acce + 8 * acc);
+                signal_tile_part<TT_MAX>(p, tc, lane);
             } else if (p.split == 1) {
 #pragma unroll 1
                 for (int c = 0; c < TT_MAX / 16; ++c) {
@@ -558,6 +587,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_acce + 8 * acc);
+                signal_tile_part<TT_MAX>(p, tc, lane);
             } else {
                 // split-K.  The 4 epilogue warps pass the same named-barrier
                 // sequence on every unit, even after a timeout (then they skip

@@ -16,6 +16,8 @@ using namespace nvfp4gg;
 
 // Device error word (one per device that loads the library).
 static __device__ int g_error_word;
+// Per-expert tile-part counters of the completion-signal entry point.
+static __device__ int g_signal_counts[NVFP4GG_MAX_GROUPS];
 
 namespace {
 
@@ -302,6 +304,21 @@ long long decode_tile_bound(int G, int M_max, int N) {
     return (long long)G * ((M_max + kNarrowTT - 1) / kNarrowTT) * ((N + 127) / 128);
 }
 
+// Device address of this device's signal counters (looked up once per device).
+int* g_signal_addr[kMaxDevices] = {};
+int signal_counts(int** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4GG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_signal_addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_signal_counts) != cudaSuccess || !ptr) return NVFP4GG_ERR_CUDA;
+        g_signal_addr[dev] = static_cast<int*>(ptr);
+    }
+    *out = g_signal_addr[dev];
+    return NVFP4GG_OK;
+}
+
 size_t splitk_part_bytes(long long tiles, int split) {
     return (size_t)tiles * split * kNarrowTT * 128 * sizeof(float);
 }
@@ -317,7 +334,8 @@ int auto_split(DeviceState* d, long long tiles, int K) {
 
 int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf, const float* alpha,
                 const int* masked_m, void* C, int G, int M_max, int N, int K, int split,
-                float* ws_part, int* ws_cnt, void* stream, bool swiglu = false) {
+                float* ws_part, int* ws_cnt, void* stream, bool swiglu = false,
+                int* signals = nullptr) {
     if (!A || !A_sf || !B || !B_sf || !alpha || !masked_m || !C) return NVFP4GG_ERR_NULL;
     int rc = check_gemm_shape(G, M_max, N, K);
     if (rc != NVFP4GG_OK) return rc;
@@ -328,7 +346,7 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
     if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
 
     const bool narrow = M_max <= 64;
-    const bool pair = !narrow && !swiglu && N % 256 == 0 &&
+    const bool pair = !narrow && !swiglu && !signals && N % 256 == 0 &&
                       (g_pair_mode == 1 || (g_pair_mode == 2 && M_max <= kPairAutoMaxRows));
     const int tt_max = narrow ? kNarrowTT : pair ? kPairTT : kWideTT;
     GemmParams p;
@@ -358,6 +376,14 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
         p.ws_part = ws_part;
         p.ws_cnt = ws_cnt;
     }
+    if (signals) {
+        int* counts = nullptr;
+        if ((rc = signal_counts(&counts)) != NVFP4GG_OK) return rc;
+        if (cudaMemsetAsync(counts, 0, (size_t)G * sizeof(int), st) != cudaSuccess)
+            return NVFP4GG_ERR_CUDA;
+        p.signals = signals;
+        p.sig_cnt = counts;
+    }
     if (swiglu)
         return narrow ? launch_variant<kNarrowTT, kNarrowStages, true>(d, 3, p, st)
                       : launch_variant<kWideTT, kWideStages, true>(d, 4, p, st);
@@ -375,6 +401,16 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
                                  int N, int K, void* stream) {
     return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr, nullptr,
                        stream);
+}
+
+int nvfp4_grouped_gemm_nt_masked_signals(const void* A, const void* A_sf, const void* B,
+                                         const void* B_sf, const float* alpha, const int* masked_m,
+                                         void* C, int G, int M_max, int N, int K, int* dst_signals,
+                                         void* stream) {
+    if (!dst_signals) return NVFP4GG_ERR_NULL;
+    if (!aligned(dst_signals, 4)) return NVFP4GG_ERR_ALIGN;
+    return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr, nullptr,
+                       stream, false, dst_signals);
 }
 
 int nvfp4_grouped_gemm_nt_masked_swiglu(const void* A, const void* A_sf, const void* B,

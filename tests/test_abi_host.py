@@ -170,3 +170,14 @@ def test_swiglu_argument_checks(lib):
     p = lib.nvfp4_prepare_weights_swiglu
     assert p(FAKE, FAKE, 2, 192, 512, FAKE + 4096, FAKE + 8192, None) == binding.ERR_SHAPE
     assert p(None, FAKE, 2, 256, 512, FAKE + 4096, FAKE + 8192, None) == binding.ERR_NULL
+
+
+def test_signals_argument_checks(lib):
+    f = lib.nvfp4_grouped_gemm_nt_masked_signals
+    args = [FAKE] * 7 + [2, 16, 256, 512, FAKE, None]
+    a = list(args); a[11] = None
+    assert f(*a) == binding.ERR_NULL
+    a = list(args); a[11] = FAKE + 2
+    assert f(*a) == binding.ERR_ALIGN
+    a = list(args); a[10] = 100
+    assert f(*a) == binding.ERR_SHAPE
