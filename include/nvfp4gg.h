@@ -177,6 +177,28 @@ int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(const void* A, const void* A_sf,
                                                 int N, int K, int split_k, void* stream);
 
 /*
+ * The GEMM on the packed-rows ("contiguous") grouped layout: the activations
+ * and the output hold only valid rows, expert after expert, instead of M_max
+ * rows per expert.  Expert g's rows start at row off[g] = masked_m[0] + ... +
+ * masked_m[g-1] (computed on the device from masked_m).
+ *   A        device u8 [M_total][K/2], A_sf device u8 [M_total][K/16]
+ *   C        device bf16 [M_total][N]; rows off[g] .. off[g] + masked_m[g] - 1
+ *            are written, no other row
+ *   M_max    bound on every masked_m[g] (picks the kernel family; values above
+ *            it are clamped and flagged NVFP4GG_ERR_MASK), M_max <= M_total
+ *   M_total  rows of A, A_sf and C (1 .. 2^24); a sum of masked_m above it is
+ *            flagged NVFP4GG_ERR_MASK and rows past M_total are not written
+ * Other arguments as in nvfp4_grouped_gemm_nt_masked (same prepared weights).
+ * The pages name this layout for a grouped baseline (DeepGEMM's contiguous
+ * grouped GEMM, in the kernel table of the page listing Helion's
+ * pretuned_kernels directory); the operation is the same.
+ */
+int nvfp4_grouped_gemm_nt_contiguous(const void* A, const void* A_sf, const void* B,
+                                     const void* B_sf, const float* alpha, const int* masked_m,
+                                     void* C, int G, int M_max, int M_total, int N, int K,
+                                     void* stream);
+
+/*
  * The GEMM with per-expert completion signals: the dst_signals argument of
  * grouped_gemm_nt_masked on "The CuteDSL Gamble: Chasing Kernel Efficiency
  * on Blackwell GPUs" ("The Message"), whose behaviour the page does not

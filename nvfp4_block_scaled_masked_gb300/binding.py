@@ -33,6 +33,7 @@ EXPORTS = (
     "nvfp4_splitk_workspace_bytes",
     "nvfp4_grouped_gemm_nt_masked_splitk",
     "nvfp4_grouped_gemm_nt_masked_splitk_noalloc",
+    "nvfp4_grouped_gemm_nt_contiguous",
     "nvfp4_grouped_gemm_nt_masked_signals",
     "nvfp4_prepare_weights_swiglu",
     "nvfp4_grouped_gemm_nt_masked_swiglu",
@@ -80,6 +81,8 @@ def load():
     lib.nvfp4_grouped_gemm_nt_masked_splitk.restype = i
     lib.nvfp4_grouped_gemm_nt_masked_splitk_noalloc.argtypes = [vp] * 7 + [i] * 5 + [vp]
     lib.nvfp4_grouped_gemm_nt_masked_splitk_noalloc.restype = i
+    lib.nvfp4_grouped_gemm_nt_contiguous.argtypes = [vp] * 7 + [i] * 5 + [vp]
+    lib.nvfp4_grouped_gemm_nt_contiguous.restype = i
     lib.nvfp4_grouped_gemm_nt_masked_signals.argtypes = [vp] * 7 + [i] * 4 + [vp, vp]
     lib.nvfp4_grouped_gemm_nt_masked_signals.restype = i
     lib.nvfp4_prepare_weights_swiglu.argtypes = [vp, vp, i, i, i, vp, vp, vp]
@@ -165,6 +168,14 @@ def nvfp4_grouped_gemm_nt_masked(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max,
                                                _ptr(alpha), _ptr(masked_m), _ptr(C),
                                                G, M_max, N, K, _stream(stream)),
            "nvfp4_grouped_gemm_nt_masked")
+
+
+def nvfp4_grouped_gemm_nt_contiguous(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, M_total,
+                                     N, K, stream=None):
+    _check(load().nvfp4_grouped_gemm_nt_contiguous(
+        _ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf), _ptr(alpha), _ptr(masked_m), _ptr(C),
+        G, M_max, M_total, N, K, _stream(stream)),
+        "nvfp4_grouped_gemm_nt_contiguous")
 
 
 def nvfp4_grouped_gemm_nt_masked_signals(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K,

@@ -79,7 +79,20 @@ struct GemmParams {
     // sig_cnt[G] counts finished tile parts (zero at kernel start)
     int* signals;
     int* sig_cnt;
+    // packed-rows layout (contiguous != 0): A, A_sf and C hold only valid
+    // rows, expert g's from row off[g] = sum_{h<g} masked_m[h], M_total rows
+    // in all; token tensor maps are over [M_total] rows with one group
+    int contiguous;
+    int M_total;
 };
+
+// Row of C holding token `tok` of expert g: g * M_max + tok in the masked
+// layout; off[g] + tok in the packed-rows layout, -1 past its M_total rows.
+__device__ __forceinline__ long long out_row(const GemmParams& p, const int* off, int g, int tok) {
+    if (!p.contiguous) return (long long)g * p.M_max + tok;
+    const int r = off[g] + tok;
+    return r < p.M_total ? r : -1;
+}
 
 // K stages [kb, ke) of split range sp of S over KS stages (balanced).
 __device__ __forceinline__ void k_range(int sp, int S, int KS, int& kb, int& ke) {
@@ -130,8 +143,9 @@ struct KCfg {
     static constexpr int NUM_BARS = 4 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_TAB = (OFF_MISC + 16 + 15) & ~15;
-    // cum[kGroupsMax + 1] (tile prefix), gm[kGroupsMax] (clamped masked_m)
-    static constexpr int TAB_BYTES = (2 * kGroupsMax + 1) * 4;
+    // cum[kGroupsMax + 1] (tile prefix), gm[kGroupsMax] (clamped masked_m),
+    // off[kGroupsMax + 1] (row prefix, packed-rows layout)
+    static constexpr int TAB_BYTES = (3 * kGroupsMax + 2) * 4;
     static constexpr int SMEM_BYTES = OFF_TAB + TAB_BYTES + 1024;   // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
@@ -250,6 +264,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
     volatile int* epi_stop = reinterpret_cast<volatile int*>(misc + 3);   // split-K: leave the loop
     int* cum = reinterpret_cast<int*>(sbase + Cfg::OFF_TAB);
     int* gm = cum + kGroupsMax + 1;
+    int* off = gm + kGroupsMax;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -298,9 +313,9 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         for (int g = lo; g < hi; ++g) sum += token_tiles<TT_MAX>(gm[g]) * p.NT;
         int incl = sum;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += v;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
         }
         int run = incl - sum;
         for (int g = lo; g < hi; ++g) {
@@ -308,6 +323,24 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
             run += token_tiles<TT_MAX>(gm[g]) * p.NT;
         }
         if (lane == 31) cum[p.G] = incl;
+        // row offsets of the packed-rows layout
+        int rs = 0;
+        for (int g = lo; g < hi; ++g) rs += gm[g];
+        int rincl = rs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, rincl, o);
+            if (lane >= o) rincl += v;
+        }
+        int rrun = rincl - rs;
+        for (int g = lo; g < hi; ++g) {
+            off[g] = rrun;
+            rrun += gm[g];
+        }
+        if (lane == 31) {
+            off[p.G] = rincl;
+            if (p.contiguous && rincl > p.M_total) record_error(p.err, NVFP4GG_ERR_MASK);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -356,11 +389,13 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                                    wq_tile + (size_t)ks * Cfg::W_TILE, Cfg::W_TILE, fb, pol_stream);
                 } else {
                     mbar_arrive_expect_tx(sb, tc.w * 16);
+                    const int ty = p.contiguous ? off[tc.g] + tc.t0 : tc.t0;
+                    const int tz = p.contiguous ? 0 : tc.g;
                     tma_load_3d(base + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN, &p.tm_asf[box], sb,
-                                ks * 16, tc.t0, tc.g);
+                                ks * 16, ty, tz);
                     mbar_arrive_expect_tx(fb, tc.w * 128);
                     tma_load_3d(base + Cfg::OFF_T + s * Cfg::T_TILE, &p.tm_a[box], fb, ks * 128,
-                                tc.t0, tc.g);
+                                ty, tz);
                 }
                 __syncwarp();
                 ++issued;
@@ -554,8 +589,9 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                     const int t = lane >> 1, hh = lane & 1;
                     const int tok = tc.t0 + c * 16 + t;
                     const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + t * 32 + hh * 16);
-                    if (tok < t_end && oc0 < NO)
-                        *reinterpret_cast<uint4*>(p.C + ((size_t)tc.g * p.M_max + tok) * NO + oc0 + 8 * hh) = v;
+                    const long long row = out_row(p, off, tc.g, tok);
+                    if (tok < t_end && oc0 < NO && row >= 0)
+                        *reinterpret_cast<uint4*>(p.C + row * NO + oc0 + 8 * hh) = v;
                     __syncwarp();
                 }
                 tc_fence_before();
@@ -579,8 +615,9 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                         const int t = tr + 8 * h;
                         const int tok = tc.t0 + c * 16 + t;
                         const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + t * 64 + tq * 16);
-                        if (tok < t_end && n_ok)
-                            *reinterpret_cast<uint4*>(p.C + ((size_t)tc.g * p.M_max + tok) * p.N + n0 + 8 * tq) = v;
+                        const long long row = out_row(p, off, tc.g, tok);
+                        if (tok < t_end && n_ok && row >= 0)
+                            *reinterpret_cast<uint4*>(p.C + row * p.N + n0 + 8 * tq) = v;
                     }
                     __syncwarp();
                 }
@@ -637,8 +674,9 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                             const int t = tr + 8 * h;
                             const int tok = tc.t0 + c * 16 + t;
                             const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + t * 64 + tq * 16);
-                            if (tok < t_end && n_ok)
-                                *reinterpret_cast<uint4*>(p.C + ((size_t)tc.g * p.M_max + tok) * p.N + n0 + 8 * tq) = v;
+                            const long long row = out_row(p, off, tc.g, tok);
+                            if (tok < t_end && n_ok && row >= 0)
+                                *reinterpret_cast<uint4*>(p.C + row * p.N + n0 + 8 * tq) = v;
                         }
                         __syncwarp();
                     }

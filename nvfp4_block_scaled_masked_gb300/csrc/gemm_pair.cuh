@@ -75,7 +75,7 @@ struct PairCfg {
     static constexpr int NUM_BARS = 4 * STAGES + 2 * ACC_BUFS + 1;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_TAB = (OFF_MISC + 16 + 15) & ~15;
-    static constexpr int TAB_BYTES = (2 * kGroupsMax + 1) * 4;
+    static constexpr int TAB_BYTES = (3 * kGroupsMax + 2) * 4;   // cum, gm, off (as the single-CTA kernel)
     static constexpr int SMEM_BYTES = OFF_TAB + TAB_BYTES + 1024;
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
     static_assert(OFF_T % 1024 == 0 && T_TILE % 1024 == 0, "128-byte swizzle alignment");
@@ -130,6 +130,7 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int* cum = reinterpret_cast<int*>(sbase + Cfg::OFF_TAB);
     int* gm = cum + kGroupsMax + 1;
+    int* off = gm + kGroupsMax;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -174,9 +175,9 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
         for (int g = lo; g < hi; ++g) sum += token_tiles<TT_MAX>(gm[g]) * NP;
         int incl = sum;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += v;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
         }
         int run = incl - sum;
         for (int g = lo; g < hi; ++g) {
@@ -184,6 +185,23 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
             run += token_tiles<TT_MAX>(gm[g]) * NP;
         }
         if (lane == 31) cum[p.G] = incl;
+        int rs = 0;
+        for (int g = lo; g < hi; ++g) rs += gm[g];
+        int rincl = rs;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, rincl, o);
+            if (lane >= o) rincl += v;
+        }
+        int rrun = rincl - rs;
+        for (int g = lo; g < hi; ++g) {
+            off[g] = rrun;
+            rrun += gm[g];
+        }
+        if (lane == 31) {
+            off[p.G] = rincl;
+            if (p.contiguous && rincl > p.M_total) record_error(p.err, NVFP4GG_ERR_MASK);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -227,11 +245,13 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
                                    wq_tile + (size_t)ks * Cfg::W_TILE, Cfg::W_TILE, fb, pol_stream);
                 } else {
                     mbar_arrive_expect_tx(sb, tc.w * 16);
+                    const int ty = p.contiguous ? off[tc.g] + tc.t0 : tc.t0;
+                    const int tz = p.contiguous ? 0 : tc.g;
                     tma_load_3d(base + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN, &p.tm_asf[(tc.w >> 4) - 1],
-                                sb, ks * 16, tc.t0, tc.g);
+                                sb, ks * 16, ty, tz);
                     mbar_arrive_expect_tx(fb, half * 128);
                     tma_load_3d(base + Cfg::OFF_T + s * Cfg::T_TILE, &p.tm_a[(half >> 4) - 1], fb,
-                                ks * 128, tc.t0 + (int)rank * half, tc.g);
+                                ks * 128, ty + (int)rank * half, tz);
                 }
                 __syncwarp();
                 ++issued;
@@ -401,8 +421,9 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
                     const int t = tr + 8 * h;
                     const int tok = tc.t0 + c * 16 + t;
                     const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + t * 64 + tq * 16);
-                    if (tok < t_end && n_ok)
-                        *reinterpret_cast<uint4*>(p.C + ((size_t)tc.g * p.M_max + tok) * p.N + n0 + 8 * tq) = v;
+                    const long long row = out_row(p, off, tc.g, tok);
+                    if (tok < t_end && n_ok && row >= 0)
+                        *reinterpret_cast<uint4*>(p.C + row * p.N + n0 + 8 * tq) = v;
                 }
                 __syncwarp();
             }

@@ -335,7 +335,7 @@ int auto_split(DeviceState* d, long long tiles, int K) {
 int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf, const float* alpha,
                 const int* masked_m, void* C, int G, int M_max, int N, int K, int split,
                 float* ws_part, int* ws_cnt, void* stream, bool swiglu = false,
-                int* signals = nullptr) {
+                int* signals = nullptr, int M_total = 0) {
     if (!A || !A_sf || !B || !B_sf || !alpha || !masked_m || !C) return NVFP4GG_ERR_NULL;
     int rc = check_gemm_shape(G, M_max, N, K);
     if (rc != NVFP4GG_OK) return rc;
@@ -351,7 +351,12 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
     const int tt_max = narrow ? kNarrowTT : pair ? kPairTT : kWideTT;
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
-    if ((rc = token_maps(A, A_sf, G, M_max, K, tt_max, p.tm_a, p.tm_asf)) != NVFP4GG_OK) return rc;
+    // packed rows (M_total > 0): one group of M_total rows; else [G][M_max]
+    if ((rc = M_total > 0 ? token_maps(A, A_sf, 1, M_total, K, tt_max, p.tm_a, p.tm_asf)
+                          : token_maps(A, A_sf, G, M_max, K, tt_max, p.tm_a, p.tm_asf)) != NVFP4GG_OK)
+        return rc;
+    p.contiguous = M_total > 0 ? 1 : 0;
+    p.M_total = M_total;
     p.wq = static_cast<const uint8_t*>(B);
     p.wsf = static_cast<const uint8_t*>(B_sf);
     p.alpha = alpha;
@@ -401,6 +406,15 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
                                  int N, int K, void* stream) {
     return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr, nullptr,
                        stream);
+}
+
+int nvfp4_grouped_gemm_nt_contiguous(const void* A, const void* A_sf, const void* B,
+                                     const void* B_sf, const float* alpha, const int* masked_m,
+                                     void* C, int G, int M_max, int M_total, int N, int K,
+                                     void* stream) {
+    if (M_total < 1 || M_total > (1 << 24) || M_max > M_total) return NVFP4GG_ERR_SHAPE;
+    return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr, nullptr,
+                       stream, false, nullptr, M_total);
 }
 
 int nvfp4_grouped_gemm_nt_masked_signals(const void* A, const void* A_sf, const void* B,

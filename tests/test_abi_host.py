@@ -181,3 +181,16 @@ def test_signals_argument_checks(lib):
     assert f(*a) == binding.ERR_ALIGN
     a = list(args); a[10] = 100
     assert f(*a) == binding.ERR_SHAPE
+
+
+def test_contiguous_argument_checks(lib):
+    f = lib.nvfp4_grouped_gemm_nt_contiguous
+    args = [FAKE] * 7 + [4, 32, 64, 256, 512, None]
+    a = list(args); a[9] = 0                      # M_total < 1
+    assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[8] = 65                     # M_max > M_total
+    assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[10] = 100                   # N % 16 != 0
+    assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[6] = None
+    assert f(*a) == binding.ERR_NULL
