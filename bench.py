@@ -262,7 +262,15 @@ def main():
     ws, rank, local = dist_setup()
 
     if args.impl == "reference":
+        if cfg.kind != "gemm":
+            if rank == 0:
+                print(json.dumps({"impl": "reference", "unavailable":
+                                  "the reference arm times the grouped GEMM workloads only"}))
+            return
         run_reference(args, cfg, ws, rank)
+        return
+    if cfg.kind == "gemv_w4a16":
+        bench_gemv(args, cfg, ws, rank, local)
         return
 
     import torch
@@ -427,6 +435,121 @@ def main():
 
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, d, prob)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def bench_gemv(args, cfg, ws, rank, local):
+    """The W4A16 decode GEMV (nvfp4_gemv_w4a16): same timing rules and JSON
+    line as the GEMM; HBM roofline over its algorithmic bytes (weights and
+    scales once, the bf16 tokens and outputs)."""
+    import torch
+    from nvfp4_block_scaled_masked_gb300 import binding, build
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    build.build()
+    binding.load()
+    peaks = load_peaks()
+    d = W.generate_gemv(cfg)
+    M, N, K = cfg.M_max, cfg.N, cfg.K
+    flops = 2.0 * M * N * K
+    nbytes = N * (K // 2 + K // 16) + M * K * 2 + M * N * 2
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    x, B, Bsf, al = dev(d["x"].view(np.int16)), dev(d["B"]), dev(d["B_sf"]), dev(d["alpha"])
+    y = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        binding.nvfp4_gemv_w4a16(x, B, Bsf, al, y, M, N, K)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(args.warmup):
+        step()
+    if binding.nvfp4_gg_check_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.mark_on()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        flush_l2(flush, i)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    sampler.mark_off()
+    sampler.stop()
+    if binding.nvfp4_gg_check_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    ms = 1e3 * replica_seconds(sum(step_ms) / 1e3, ws) / args.steps
+    gbs = nbytes / (ms / 1e3) / 1e9
+    # end to end: pinned tokens in, GEMV, outputs back, every step
+    hx = torch.from_numpy(d["x"].view(np.int16).copy()).pin_memory()
+    hy = torch.empty((M, N), dtype=torch.int16).pin_memory()
+
+    def e2e_step():
+        x.copy_(hx, non_blocking=True)
+        step()
+        hy.copy_(y, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for i in range(args.e2e_steps):
+        flush_l2(flush, i)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        e2e_step()
+        stream.synchronize()
+        e2e_ms.append(1e3 * (time.perf_counter() - t1))
+    e2e_med = statistics.median(e2e_ms)
+    line = {
+        "metric": METRIC, "value": flops * ws / (ms / 1e3) / 1e12, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "nvfp4 weights (e2m1, e4m3 block-16 scales) x bf16 activations, f32 accumulate, bf16 out",
+        "data": "synthetic",
+        "config": {"workload": cfg.name, "M": M, "N": N, "K": K, "seed": hex(cfg.seed),
+                   "parallelism": "replicas",
+                   "l2": "flushed between steps: 256 MB written, then read back (clean L2)"},
+        "algorithmic_gbs": gbs, "gpu_launches": args.steps, "entry_point": "nvfp4_gemv_w4a16",
+        "wall_s_timed_region": wall,
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm"], "traffic": profiled_traffic(cfg.key),
+                     "algorithmic_bytes": nbytes, "peak_note": f"HBM copy bandwidth, {peaks['src']}"},
+        "e2e": {"value": flops / (e2e_med / 1e3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": M * K * 2, "d2h_bytes_per_step": M * N * 2,
+                "ms_per_step": e2e_med, "steps": args.e2e_steps,
+                "how": "pinned tokens copied in, nvfp4_gemv_w4a16, outputs copied back, stream "
+                       "sync; wall clock per step (Python call included)"},
+        "clocks": sampler.summary(),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import oracle
+        t1 = time.perf_counter()
+        _, ref = oracle.gemv_w4a16(d["x"], d["B"], d["B_sf"], d["alpha"][0], K)
+        el = time.perf_counter() - t1
+        vals = (y.cpu().numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+        ok = oracle.tolerance_ok(vals, ref, np.abs(ref).max())
+        line["cpu_baseline"] = {"value": flops / el / 1e12, "unit": UNIT, "cores": os.cpu_count(),
+                                "kind": "oracle", "sample": f"the whole GEMV (M={M}, N={N}, K={K}), fp64",
+                                "seconds": el,
+                                "parity": {"outputs": int(ok.size), "within_tolerance": int(ok.sum())}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:

@@ -177,6 +177,25 @@ int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(const void* A, const void* A_sf,
                                                 int N, int K, int split_k, void* stream);
 
 /*
+ * W4A16 GEMV for decode: NVFP4 weights, bf16 activations, the "nvfp4_gemv"
+ * workload (W4A16) in the kernel table of the page listing Helion's
+ * pretuned_kernels directory ("Decode (M=1) NVFP4 GEMV (N, K) weight
+ * shapes").  For m < M, n < N:
+ *     y[m][n] = bf16( alpha[0] * sum_k x[m][k] * B[n][k] )     (fp32 accumulation)
+ *   x      device bf16 [M][K], 16-byte aligned
+ *   B      device u8 [N][K/2] e2m1 codes, the raw row-major layout (no
+ *          nvfp4_prepare_weights), 16-byte aligned
+ *   B_sf   device u8 [N][K/16] e4m3 scales, row-major
+ *   alpha  device f32 [1]
+ *   y      device bf16 [M][N]
+ * Limits: 1 <= M <= 8, K % 32 == 0, M * K <= 43690 (the tokens are staged
+ * in shared memory as fp32), N <= 2^24.  The W4A4 form (NVFP4 activations)
+ * is nvfp4_grouped_gemm_nt_masked with G = 1.
+ */
+int nvfp4_gemv_w4a16(const void* x, const void* B, const void* B_sf, const float* alpha, void* y,
+                     int M, int N, int K, void* stream);
+
+/*
  * The GEMM on the packed-rows ("contiguous") grouped layout: the activations
  * and the output hold only valid rows, expert after expert, instead of M_max
  * rows per expert.  Expert g's rows start at row off[g] = masked_m[0] + ... +

@@ -34,6 +34,7 @@ EXPORTS = (
     "nvfp4_grouped_gemm_nt_masked_splitk",
     "nvfp4_grouped_gemm_nt_masked_splitk_noalloc",
     "nvfp4_grouped_gemm_nt_contiguous",
+    "nvfp4_gemv_w4a16",
     "nvfp4_grouped_gemm_nt_masked_signals",
     "nvfp4_prepare_weights_swiglu",
     "nvfp4_grouped_gemm_nt_masked_swiglu",
@@ -81,6 +82,8 @@ def load():
     lib.nvfp4_grouped_gemm_nt_masked_splitk.restype = i
     lib.nvfp4_grouped_gemm_nt_masked_splitk_noalloc.argtypes = [vp] * 7 + [i] * 5 + [vp]
     lib.nvfp4_grouped_gemm_nt_masked_splitk_noalloc.restype = i
+    lib.nvfp4_gemv_w4a16.argtypes = [vp] * 5 + [i] * 3 + [vp]
+    lib.nvfp4_gemv_w4a16.restype = i
     lib.nvfp4_grouped_gemm_nt_contiguous.argtypes = [vp] * 7 + [i] * 5 + [vp]
     lib.nvfp4_grouped_gemm_nt_contiguous.restype = i
     lib.nvfp4_grouped_gemm_nt_masked_signals.argtypes = [vp] * 7 + [i] * 4 + [vp, vp]
@@ -168,6 +171,12 @@ def nvfp4_grouped_gemm_nt_masked(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max,
                                                _ptr(alpha), _ptr(masked_m), _ptr(C),
                                                G, M_max, N, K, _stream(stream)),
            "nvfp4_grouped_gemm_nt_masked")
+
+
+def nvfp4_gemv_w4a16(x, B, B_sf, alpha, y, M, N, K, stream=None):
+    _check(load().nvfp4_gemv_w4a16(_ptr(x), _ptr(B), _ptr(B_sf), _ptr(alpha), _ptr(y), M, N, K,
+                                   _stream(stream)),
+           "nvfp4_gemv_w4a16")
 
 
 def nvfp4_grouped_gemm_nt_contiguous(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, M_total,

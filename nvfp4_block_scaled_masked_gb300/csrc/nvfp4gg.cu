@@ -10,6 +10,7 @@
 
 #include "gemm.cuh"
 #include "gemm_pair.cuh"
+#include "gemv.cuh"
 #include "nvfp4gg.h"
 
 using namespace nvfp4gg;
@@ -406,6 +407,68 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
                                  int N, int K, void* stream) {
     return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr, nullptr,
                        stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+template <int M>
+int launch_gemv(DeviceState* d, const void* x, const void* B, const void* B_sf, const float* alpha,
+                void* y, int N, int K, cudaStream_t st) {
+    auto kern = gemv_w4a16_kernel<M>;
+    const int smem = M * (K / 32) * kGemvRow * (int)sizeof(float);
+    static bool attr_done[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4GG_ERR_CUDA;
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kGemvMaxSmem) != cudaSuccess)
+            return NVFP4GG_ERR_CUDA;
+        attr_done[dev] = true;
+    }
+    // as many CTAs per SM as registers and the staged tokens allow (more
+    // warps, more loads in flight), row pairs grid-strided over all warps
+    int per_sm = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGemvThreads, smem) !=
+            cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    const long long need = (((long long)N + 1) / 2 * 32 + kGemvThreads - 1) / kGemvThreads;
+    long long grid = (long long)per_sm * d->sms;
+    if (grid > need) grid = need;
+    kern<<<(int)grid, kGemvThreads, smem, st>>>(
+        static_cast<const __nv_bfloat16*>(x), static_cast<const uint8_t*>(B),
+        static_cast<const uint8_t*>(B_sf), alpha, static_cast<__nv_bfloat16*>(y), N, K);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+extern "C" {
+
+int nvfp4_gemv_w4a16(const void* x, const void* B, const void* B_sf, const float* alpha, void* y,
+                     int M, int N, int K, void* stream) {
+    if (!x || !B || !B_sf || !alpha || !y) return NVFP4GG_ERR_NULL;
+    if (M < 1 || M > kGemvMaxTokens || N < 1 || N > (1 << 24) || K < 32 || K % 32 != 0 ||
+        (long long)M * (K / 32) * kGemvRow * 4 > kGemvMaxSmem)
+        return NVFP4GG_ERR_SHAPE;
+    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(B_sf, 2) || !aligned(y, 2) ||
+        !aligned(alpha, 4))
+        return NVFP4GG_ERR_ALIGN;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != NVFP4GG_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    switch (M) {
+        case 1: return launch_gemv<1>(d, x, B, B_sf, alpha, y, N, K, st);
+        case 2: return launch_gemv<2>(d, x, B, B_sf, alpha, y, N, K, st);
+        case 3: return launch_gemv<3>(d, x, B, B_sf, alpha, y, N, K, st);
+        case 4: return launch_gemv<4>(d, x, B, B_sf, alpha, y, N, K, st);
+        case 5: return launch_gemv<5>(d, x, B, B_sf, alpha, y, N, K, st);
+        case 6: return launch_gemv<6>(d, x, B, B_sf, alpha, y, N, K, st);
+        case 7: return launch_gemv<7>(d, x, B, B_sf, alpha, y, N, K, st);
+        default: return launch_gemv<8>(d, x, B, B_sf, alpha, y, N, K, st);
+    }
 }
 
 int nvfp4_grouped_gemm_nt_contiguous(const void* A, const void* A_sf, const void* B,

@@ -51,6 +51,7 @@ class Config:
     tokens: int = 0               # for "topk"
     topk: int = 0
     alpha_one: bool = False
+    kind: str = "gemm"            # "gemm" | "gemv_w4a16" (M_max tokens of bf16 activations)
 
     @property
     def seed(self) -> int:
@@ -80,7 +81,30 @@ EXTRA = {
                  "fixed", masked_list=(0,) * 32),
     "x1": Config("x1", "decode GEMM1 one expert G=1 masked_m=7 N=4096 K=7168", 1, 16, 4096, 7168,
                  "fixed", masked_list=(7,)),
+    # W4A16 decode GEMV, one token, Llama-3-8B MLP projection shapes (the
+    # pages' nvfp4_gemv workload names Llama-3 / Qwen projections)
+    "v1": Config("v1", "decode GEMV W4A16 M=1 N=14336 K=4096", 1, 1, 14336, 4096,
+                 "fixed", masked_list=(1,), kind="gemv_w4a16"),
+    "v2": Config("v2", "decode GEMV W4A16 M=1 N=4096 K=14336", 1, 1, 4096, 14336,
+                 "fixed", masked_list=(1,), kind="gemv_w4a16"),
 }
+
+
+def generate_gemv(cfg: Config, seed: int | None = None) -> dict:
+    """Inputs of the W4A16 GEMV: x bf16 bits u16[M, K] (M = cfg.M_max) built
+    directly as bf16 patterns (random sign, exponent 2^-3 .. 2^1, 7-bit
+    mantissa: no rounding), B u8[N, K/2] and B_sf u8[N, K/16] in the raw layout
+    drawn like the GEMM's weights, alpha f32 uniform in [0.5, 2)."""
+    rng = np.random.default_rng(cfg.seed if seed is None else seed)
+    M, N, K = cfg.M_max, cfg.N, cfg.K
+    sign = rng.integers(0, 2, (M, K)).astype(np.uint16)
+    exp = rng.integers(127 - 3, 127 + 2, (M, K)).astype(np.uint16)
+    man = rng.integers(0, 128, (M, K)).astype(np.uint16)
+    x = (sign << 15) | (exp << 7) | man
+    alpha = np.float32(rng.uniform(0.5, 2.0))
+    B = draw_codes(rng, (N, K // 2))
+    B_sf = draw_scales(rng, (N, K // 16))
+    return dict(cfg=cfg, x=x.astype(np.uint16), B=B, B_sf=B_sf, alpha=np.array([alpha], np.float32))
 
 
 def lookup(key: str) -> Config:

@@ -10,6 +10,8 @@ Two implementations live here, written independently of each other:
   fp64, built with gcc (OpenMP over independent output rows only).
 * ``gemm_numpy`` is a second, NumPy fp64 restatement used to cross-check the
   C oracle on small shapes (table lookup, scale broadcast, ``einsum``).
+* ``gemv_w4a16`` is the decode GEMV with bf16 activations, the plain fp64
+  product of the decoded weights and the activations.
 * ``swiglu`` applies the MoE block's SwiGLU step to GEMM1's unrounded fp64
   output (``silu(gate) * up``, one bf16 rounding), for the fused GEMM1
   epilogue.
@@ -268,6 +270,18 @@ def swiglu(ref64, masked_m, C_init_half):
         out[g, :m] = y
         C[g, :m] = bf16_bits_any(y)
     return C, out
+
+
+def gemv_w4a16(x_bits, B, B_sf, alpha, K):
+    """The W4A16 decode GEMV ("nvfp4_gemv", W4A16, in the kernel table of the
+    page listing Helion's pretuned_kernels directory): y[m, n] = alpha *
+    sum_k x[m, k] * B[n, k], x bf16 (bits uint16 [M, K]), B NVFP4 in the raw
+    layout (codes [N, K/2], scales [N, K/16]) decoded by decode_numpy; fp64,
+    one bf16 rounding.  Returns (y bits uint16 [M, N], y64)."""
+    xd = (np.asarray(x_bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    Bd = decode_numpy(B, B_sf, K)
+    y64 = float(alpha) * (xd @ Bd.T)
+    return bf16_bits_any(y64), y64
 
 
 def tolerance_ok(gpu_vals, ref64, max_abs):

@@ -194,3 +194,20 @@ def test_contiguous_argument_checks(lib):
     assert f(*a) == binding.ERR_SHAPE
     a = list(args); a[6] = None
     assert f(*a) == binding.ERR_NULL
+
+
+def test_gemv_argument_checks(lib):
+    f = lib.nvfp4_gemv_w4a16
+    args = [FAKE] * 5 + [1, 4096, 4096, None]
+    a = list(args); a[5] = 0
+    assert f(*a) == binding.ERR_SHAPE            # M < 1
+    a = list(args); a[5] = 9
+    assert f(*a) == binding.ERR_SHAPE            # M > 8
+    a = list(args); a[7] = 4008
+    assert f(*a) == binding.ERR_SHAPE            # K % 32 != 0
+    a = list(args); a[5] = 8; a[7] = 8192
+    assert f(*a) == binding.ERR_SHAPE            # tokens do not fit shared memory
+    a = list(args); a[1] = FAKE + 8
+    assert f(*a) == binding.ERR_ALIGN
+    a = list(args); a[4] = None
+    assert f(*a) == binding.ERR_NULL

@@ -406,3 +406,39 @@ def test_bf16_bits_any_subnormal_grid():
     vals = np.array([1.0, -2.0 ** -130, 1.5 * 2.0 ** -133, 2.5 * 2.0 ** -133, 128 * 2.0 ** -133, -0.0])
     want = torch.from_numpy(vals.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy()
     np.testing.assert_array_equal(oracle.bf16_bits_any(vals), want.astype(np.uint16))
+
+
+# ---------------------------------------------------- W4A16 decode GEMV
+
+def test_gemv_one_hot_reads_one_weight_column():
+    """x = 2^j at position k, zero elsewhere: y[n] = alpha * 2^j * code * scale
+    of weight element (n, k), from the OCP tables by hand."""
+    N, K = 4, 64
+    B = np.zeros((N, K // 2), np.uint8)
+    B_sf = np.full((N, K // 16), 0x38, np.uint8)
+    k = 37                                     # odd: high nibble of byte 18, scale block 2
+    codes = [0x5, 0xF, 0x1, 0x0]               # 3, -6, 0.5, 0
+    scales = [0x40, 0x30, 0x48, 0x38]          # 2, 0.5, 4, 1
+    for n in range(N):
+        B[n, k // 2] = codes[n] << 4
+        B_sf[n, k // 16] = scales[n]
+    x = np.zeros((1, K), np.uint16)
+    x[0, k] = 0x4000                           # 2.0
+    bits, y = oracle.gemv_w4a16(x, B, B_sf, 0.75, K)
+    np.testing.assert_array_equal(y[0], 0.75 * 2.0 * np.array([3 * 2, -6 * 0.5, 0.5 * 4, 0]))
+    want = torch.tensor(y[0], dtype=torch.float32).to(torch.bfloat16).view(torch.int16).numpy()
+    np.testing.assert_array_equal(bits[0], want.astype(np.uint16))
+
+
+def test_gemv_integer_case_is_int64_matmul():
+    rng = np.random.default_rng(5)
+    M, N, K = 3, 9, 96
+    vals = np.array([0, 1, -1, 2])
+    codes = np.array([0x0, 0x2, 0xA, 0x4], dtype=np.uint8)
+    ib = rng.integers(0, 4, (N, K))
+    B = (codes[ib[:, 0::2]] | (codes[ib[:, 1::2]] << 4)).astype(np.uint8)
+    B_sf = np.full((N, K // 16), 0x38, np.uint8)
+    xi = rng.integers(-3, 4, (M, K))
+    x = torch.from_numpy(xi.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
+    _, y = oracle.gemv_w4a16(x, B, B_sf, 1.0, K)
+    np.testing.assert_array_equal(y, (xi.astype(np.int64) @ vals[ib].T).astype(np.float64))
