@@ -179,8 +179,8 @@ int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(const void* A, const void* A_sf,
 /*
  * W4A16 GEMV for decode: NVFP4 weights, bf16 activations, the "nvfp4_gemv"
  * workload (W4A16) in the kernel table of the page listing Helion's
- * pretuned_kernels directory ("Decode (M=1) NVFP4 GEMV (N, K) weight
- * shapes").  For m < M, n < N:
+ * pretuned_kernels directory (a one-token decode GEMV over model
+ * projection shapes).  For m < M, n < N:
  *     y[m][n] = bf16( alpha[0] * sum_k x[m][k] * B[n][k] )     (fp32 accumulation)
  *   x      device bf16 [M][K], 16-byte aligned
  *   B      device u8 [N][K/2] e2m1 codes, the raw row-major layout (no
@@ -244,7 +244,7 @@ int nvfp4_grouped_gemm_nt_masked_signals(const void* A, const void* A_sf, const 
  * GEMM1 of an MoE expert block with its SwiGLU activation fused into the
  * epilogue: the step that follows this GEMM on the page "LLM-Assisted Kernel
  * Development in CuTe DSL, Gluon, Helion and Triton" (mixture-of-experts
- * section: per expert GEMM1 -> SwiGLU -> GEMM2, I = 2048).  B is GEMM1's
+ * section: each expert runs GEMM1, then SwiGLU, then GEMM2; I = 2048).  B is GEMM1's
  * weight [G][N][K] with N = 2 I: rows 0 .. I-1 the gate projection, rows
  * I .. 2I-1 the up projection (the page does not fix the order; this is the
  * reading taken).  For m < masked_m[g] and j < I:

@@ -1,7 +1,7 @@
 // W4A16 GEMV for decode (M <= 8 tokens): NVFP4 weights, bf16 activations,
-// the "nvfp4_gemv" workload (W4A16) in the kernel table of the page listing
-// Helion's pretuned_kernels directory ("Decode (M=1) NVFP4 GEMV (N, K)
-// weight shapes").  For every token m < M and weight row n < N:
+// the nvfp4_gemv workload (its W4A16 form) in the kernel table of the page
+// listing Helion's pretuned_kernels directory, a one-token decode GEMV over
+// model projection shapes.  For every token m < M and weight row n < N:
 //
 //     y[m][n] = bf16( alpha * sum_k x[m][k] * B[n][k] )
 //

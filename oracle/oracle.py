@@ -252,7 +252,7 @@ def silu(x):
 def swiglu(ref64, masked_m, C_init_half):
     """The SwiGLU step after GEMM1 in the MoE expert block of the page
     "LLM-Assisted Kernel Development in CuTe DSL, Gluon, Helion and Triton"
-    (mixture-of-experts section: per expert GEMM1 -> SwiGLU -> GEMM2).  From
+    (mixture-of-experts section: each expert runs GEMM1, SwiGLU, GEMM2).  From
     GEMM1's unrounded fp64 output ref64 [G, M_max, N] (N = 2I; reading: the
     first I columns are the gate projection, the last I the up projection):
     out[g, m, j] = silu(ref64[g, m, j]) * ref64[g, m, I + j] in fp64, rounded

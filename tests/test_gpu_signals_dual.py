@@ -3,7 +3,7 @@
 * Per-expert completion signals (nvfp4_grouped_gemm_nt_masked_signals): each
   call adds exactly 1 to every expert's signal, empty experts included, and
   C is bit-identical to the plain single-CTA call.
-* The dual GEMM (two GEMMs sharing A, on the page "LLM-Assisted Kernel
+* The dual GEMM (one A operand used by two GEMMs, on the page "LLM-Assisted Kernel
   Development in CuTe DSL, Gluon, Helion and Triton"): with B1 and B2 stacked
   along N ("merged B") one call computes both, each equal to its own oracle
   GEMM; with the SwiGLU entry point it computes silu(A B1^T) * (A B2^T)."""
@@ -69,7 +69,7 @@ def test_signals_count_once_per_call_and_results_match(lib, G, M_max, N, K, mask
 
 
 def test_dual_gemm_merged_b_and_swiglu(lib):
-    """A [M, K] shared; B1, B2 [N1, K]: the merged-B call equals the two oracle
+    """A [M, K] shared; B1, B2 [N1, K]: the call on B1 and B2 stacked equals the two oracle
     GEMMs column block by column block, and the SwiGLU call equals
     silu(A B1^T) * (A B2^T) from the same oracle outputs."""
     from nvfp4_block_scaled_masked_gb300.device import Problem
