@@ -5,7 +5,7 @@
   C is bit-identical to the plain single-CTA call.
 * The dual GEMM (one A operand used by two GEMMs, on the page "LLM-Assisted Kernel
   Development in CuTe DSL, Gluon, Helion and Triton"): with B1 and B2 stacked
-  along N ("merged B") one call computes both, each equal to its own oracle
+  along N one call computes both, each equal to its own oracle
   GEMM; with the SwiGLU entry point it computes silu(A B1^T) * (A B2^T)."""
 import numpy as np
 import pytest
