@@ -19,8 +19,9 @@
  *     b(g,n,k)   = e2m1(B code of element k of row n) * e4m3(B_sf[g][n][k/16])
  *   rows m >= masked_m[g] of C are not written.
  *
- * The pages name NVFP4 ("4-bit floating point with block-level scale factors",
- * same page, "Input Knowledge Required") but never define its encodings.  The
+ * The pages name NVFP4 (a 4-bit floating-point format with a scale per block
+ * of elements; same page, "Input Knowledge Required") but never define its
+ * encodings.  The
  * readings taken here are the public OCP Microscaling definitions:
  *   - e2m1: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa;
  *     exponent 0 is subnormal with value mantissa * 0.5.
