@@ -188,8 +188,8 @@ int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(const void* A, const void* A_sf,
  *   B_sf   device u8 [N][K/16] e4m3 scales, row-major
  *   alpha  device f32 [1]
  *   y      device bf16 [M][N]
- * Limits: 1 <= M <= 8, K % 32 == 0, M * K <= 43690 (the tokens are staged
- * in shared memory as fp32), N <= 2^24.  The W4A4 form (NVFP4 activations)
+ * Limits: 1 <= M <= 8, K % 32 == 0, M * K <= 71493 (the tokens are staged
+ * in shared memory, 2.75 bytes per value), N <= 2^24.  The W4A4 form (NVFP4 activations)
  * is nvfp4_grouped_gemm_nt_masked with G = 1.
  */
 int nvfp4_gemv_w4a16(const void* x, const void* B, const void* B_sf, const float* alpha, void* y,

@@ -9,15 +9,22 @@
 // (raw row-major layout: codes [N][K/2], scales [N][K/16]) and x, y are bf16.
 //
 // Each weight byte is read once, so the kernel streams HBM: one warp per
-// pair of weight rows (pairs grid-strided over all warps), every lane loading 16-byte
-// chunks of the row (32 codes) with coalesced, evict-first loads; the tokens
-// are staged once per CTA in shared memory as fp32, 32 values per K chunk
-// padded to 36 (lanes read different chunks: rows 144 bytes apart keep the
-// 16-byte loads of a warp free of bank conflicts).  Codes and scales are
-// converted with CUDA's fp4 / fp8 conversion intrinsics; products are summed
-// in fp32 per 16-element block and the block scale applied once; a warp
-// reduction ends the row.  No tensor cores: two FLOPs per weight byte and a
-// half cannot use them.
+// group of R weight rows (2 up to four tokens, else 1; groups grid-strided
+// over all warps), every lane loading 16-byte chunks of the row (32 codes)
+// with coalesced, evict-first loads.  The tokens are staged once per CTA in
+// shared memory as f16 with a power-of-two factor per 16-element block: the
+// block's largest value is moved to [2^14, 2^15), so every bf16 value down
+// to 2^-31 of it is exact in f16 (8 significant bits) and only smaller ones,
+// far below the fp32 accumulation error, are rounded.  32 values per K chunk
+// are padded to 80 bytes (lanes read different chunks: rows 5 x 16 bytes
+// apart keep the 16-byte loads of a warp free of bank conflicts).  Codes are
+// converted with the hardware e2m1x2 -> f16x2 conversion and multiplied with
+// mixed-precision FMAs (f16 factors, fp32 accumulator: the code-times-token
+// product is exact), so no conversion to fp32 sits on the per-code path; at
+// one token the instruction stream, not only HBM, bounds this kernel.  Block
+// scale times token factor is applied once per 16 products; a warp reduction
+// ends the row.  No tensor cores: two FLOPs per weight byte and a half cannot
+// use them.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -30,121 +37,179 @@ namespace nvfp4gg {
 
 constexpr int kGemvMaxTokens = 8;
 constexpr int kGemvThreads = 256;
-constexpr int kGemvMaxSmem = 192 * 1024;   // tokens staged as fp32: M * (K / 32) * 144 bytes
-constexpr int kGemvRow = 36;               // floats per staged 32-value chunk
+constexpr int kGemvMaxSmem = 192 * 1024;   // staged tokens: 2.75 bytes per token value
+constexpr int kGemvRowBytes = 80;          // 32 f16 tokens + 16 bytes of padding per K chunk
 constexpr int kGemvBatch = 4;              // chunks per lane and row loaded before use
 
-// Two e2m1 codes (low nibble = even element) as floats.
-__device__ __forceinline__ float2 e2m1x2_to_float2(uint32_t byte) {
-    const __half2 h = __half2(__nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(byte), __NV_E2M1));
-    return __half22float2(h);
+// shared memory of M staged tokens of K values: f16 chunks and block factors
+inline long long gemv_smem_bytes(int M, int K) {
+    return (long long)M * (K / 32) * kGemvRowBytes + (long long)M * (K / 16) * 4;
 }
 
 __device__ __forceinline__ float e4m3_to_float(uint32_t byte) {
     return __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(byte), __NV_E4M3)));
 }
 
-// Sum over the 16 codes of words w0, w1 (8 codes each) times x[0..15]
-// (16-byte aligned in shared memory).
-__device__ __forceinline__ float block16(uint32_t w0, uint32_t w1, const float* xs) {
-    const float4* x4 = reinterpret_cast<const float4*>(xs);
-    float p = 0.f;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const uint32_t w = h ? w1 : w0;
-        const float4 xa = x4[2 * h], xb = x4[2 * h + 1];
-        const float2 c0 = e2m1x2_to_float2(w & 0xFFu), c1 = e2m1x2_to_float2((w >> 8) & 0xFFu);
-        const float2 c2 = e2m1x2_to_float2((w >> 16) & 0xFFu), c3 = e2m1x2_to_float2(w >> 24);
-        p = fmaf(c0.x, xa.x, p);
-        p = fmaf(c0.y, xa.y, p);
-        p = fmaf(c1.x, xa.z, p);
-        p = fmaf(c1.y, xa.w, p);
-        p = fmaf(c2.x, xb.x, p);
-        p = fmaf(c2.y, xb.y, p);
-        p = fmaf(c3.x, xb.z, p);
-        p = fmaf(c3.y, xb.w, p);
-    }
-    return p;
+// acc + sum over the 8 codes of word w (byte j: codes 2j, 2j+1, low nibble
+// first) times the 8 f16 tokens in x01, x23, x45, x67 (two per register, low
+// half first).  e2m1x2 -> f16x2 conversions, then mixed-precision FMAs with
+// f16 factors and an fp32 accumulator: each product (at most 10 significant
+// bits) is exact, one rounding per addition, no f16 -> f32 conversions.
+__device__ __forceinline__ float dot8(uint32_t w, uint32_t x01, uint32_t x23, uint32_t x45,
+                                      uint32_t x67, float acc) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        ".reg .b32 h0, h1, h2, h3;\n\t"
+        ".reg .b16 c0, c1, c2, c3, c4, c5, c6, c7, y0, y1, y2, y3, y4, y5, y6, y7;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 h0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 h1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 h2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 h3, b3;\n\t"
+        "mov.b32 {c0, c1}, h0;\n\tmov.b32 {c2, c3}, h1;\n\t"
+        "mov.b32 {c4, c5}, h2;\n\tmov.b32 {c6, c7}, h3;\n\t"
+        "mov.b32 {y0, y1}, %2;\n\tmov.b32 {y2, y3}, %3;\n\t"
+        "mov.b32 {y4, y5}, %4;\n\tmov.b32 {y6, y7}, %5;\n\t"
+        "fma.rn.f32.f16 %0, c0, y0, %0;\n\tfma.rn.f32.f16 %0, c1, y1, %0;\n\t"
+        "fma.rn.f32.f16 %0, c2, y2, %0;\n\tfma.rn.f32.f16 %0, c3, y3, %0;\n\t"
+        "fma.rn.f32.f16 %0, c4, y4, %0;\n\tfma.rn.f32.f16 %0, c5, y5, %0;\n\t"
+        "fma.rn.f32.f16 %0, c6, y6, %0;\n\tfma.rn.f32.f16 %0, c7, y7, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(w), "r"(x01), "r"(x23), "r"(x45), "r"(x67));
+    return acc;
 }
 
-template <int M>
+// Sum over the 16 codes of words w0, w1 times the 16 staged f16 tokens at xh
+// (16-byte aligned: two 16-byte loads).
+__device__ __forceinline__ float block16(uint32_t w0, uint32_t w1, const uint4* xh) {
+    const uint4 xa = xh[0], xb = xh[1];
+    float p = dot8(w0, xa.x, xa.y, xa.z, xa.w, 0.f);
+    return dot8(w1, xb.x, xb.y, xb.z, xb.w, p);
+}
+
+// A warp's work is a sequence of items (row group, chunk batch): the loads of
+// item i + 1 are issued before the arithmetic of item i, and the first
+// item's loads before the tokens are staged, so loads and arithmetic overlap.
+template <int R>
+struct GemvBatch {
+    uint4 q[kGemvBatch][R];
+    uint32_t t[kGemvBatch][R];
+};
+
+template <int R>
+__device__ __forceinline__ void gemv_load(GemvBatch<R>& b, const uint8_t* __restrict__ B,
+                                          const uint8_t* __restrict__ B_sf, int n0, int N, int K,
+                                          int c0, int chunks) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const int n = n0 + r < N ? n0 + r : n0;   // past N: repeat row n0, not stored
+        const uint4* row = reinterpret_cast<const uint4*>(B + (size_t)n * (K >> 1));
+        const uint16_t* srow = reinterpret_cast<const uint16_t*>(B_sf + (size_t)n * (K >> 4));
+#pragma unroll
+        for (int u = 0; u < kGemvBatch; ++u) {
+            const int c = c0 + 32 * u;
+            if (c < chunks) {
+                b.q[u][r] = __ldcs(row + c);
+                b.t[u][r] = __ldcs(srow + c);
+            }
+        }
+    }
+}
+
+template <int M, int R>
 __global__ void __launch_bounds__(kGemvThreads, 2)
 gemv_w4a16_kernel(const __nv_bfloat16* __restrict__ x, const uint8_t* __restrict__ B,
                   const uint8_t* __restrict__ B_sf, const float* __restrict__ alpha,
                   __nv_bfloat16* __restrict__ y, int N, int K) {
-    extern __shared__ __align__(16) float xs[];   // [M][K/32][36] fp32
+    // tokens staged as f16 times 2^-e per 16-element block (e from the block's
+    // largest exponent), 2^e kept beside it: [M][K/32] rows of 32 halves + 8
+    // halves of padding (80 bytes), then [M][K/16] fp32 block factors
+    extern __shared__ __align__(16) uint8_t gemv_smem[];
     const int chunks = K >> 5;                 // 16-byte chunks (32 codes) per row
-    // stage the tokens: 8 bf16 per 16-byte load
-    for (int i = threadIdx.x; i < (M * K) >> 3; i += blockDim.x) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(x) + i);
-        float* dst = xs + ((i << 3) >> 5) * kGemvRow + ((i << 3) & 31);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float* xf = reinterpret_cast<float*>(gemv_smem + (size_t)M * chunks * kGemvRowBytes);
+    const int lane = threadIdx.x & 31;
+    const int wid = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int warps = (int)((gridDim.x * blockDim.x) >> 5);
+    const int groups = (N + R - 1) / R;
+    const int nbat = (chunks + 32 * kGemvBatch - 1) / (32 * kGemvBatch);   // batches per row group
+    const int mine = wid < groups ? (groups - 1 - wid) / warps + 1 : 0;    // row groups of this warp
+    const int items = mine * nbat;
+    GemvBatch<R> cur, nxt;
+    if (items > 0) gemv_load<R>(cur, B, B_sf, R * wid, N, K, lane, chunks);
+    for (int blk = threadIdx.x; blk < (M * K) >> 4; blk += blockDim.x) {
+        const uint4* src = reinterpret_cast<const uint4*>(x) + 2 * blk;
+        const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint32_t emax = 0;   // largest biased exponent of the block
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            dst[2 * j] = __uint_as_float(w[j] << 16);
-            dst[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-        }
+        for (int j = 0; j < 8; ++j)
+            emax = max(emax, max((w[j] >> 7) & 0xFFu, (w[j] >> 23) & 0xFFu));
+        // the largest value, in [2^(emax-127), 2^(emax-126)), goes to [2^14,
+        // 2^15); blocks below 2^-111 (zero, subnormal) use e = -126 instead,
+        // which keeps both factors normal fp32 powers of two
+        const int e = max((int)emax - 141, -126);
+        const float down = __uint_as_float((uint32_t)(127 - e) << 23);
+        const float up = __uint_as_float((uint32_t)(127 + e) << 23);
+        __half2 hv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            hv[j] = __floats2half2_rn(__uint_as_float(w[j] << 16) * down,
+                                      __uint_as_float(w[j] & 0xFFFF0000u) * down);
+        const int mrow = blk / (K >> 4), kb = blk - mrow * (K >> 4);   // token, 16-block
+        uint4* dst = reinterpret_cast<uint4*>(gemv_smem + ((size_t)mrow * chunks + (kb >> 1)) * kGemvRowBytes +
+                                              (kb & 1) * 32);
+        dst[0] = make_uint4(*reinterpret_cast<uint32_t*>(&hv[0]), *reinterpret_cast<uint32_t*>(&hv[1]),
+                            *reinterpret_cast<uint32_t*>(&hv[2]), *reinterpret_cast<uint32_t*>(&hv[3]));
+        dst[1] = make_uint4(*reinterpret_cast<uint32_t*>(&hv[4]), *reinterpret_cast<uint32_t*>(&hv[5]),
+                            *reinterpret_cast<uint32_t*>(&hv[6]), *reinterpret_cast<uint32_t*>(&hv[7]));
+        xf[blk] = up;
     }
     __syncthreads();
-    const int lane = threadIdx.x & 31;
-    const int warps = (int)((gridDim.x * blockDim.x) >> 5);
     const float al = __ldg(alpha);
-    // each warp streams two rows at once (twice the loads in flight)
-    for (int n0 = 2 * (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5); n0 < N; n0 += 2 * warps) {
-        const bool two = n0 + 1 < N;
-        const int n1 = two ? n0 + 1 : n0;
-        const uint4* row0 = reinterpret_cast<const uint4*>(B + (size_t)n0 * (K >> 1));
-        const uint4* row1 = reinterpret_cast<const uint4*>(B + (size_t)n1 * (K >> 1));
-        const uint16_t* srow0 = reinterpret_cast<const uint16_t*>(B_sf + (size_t)n0 * (K >> 4));
-        const uint16_t* srow1 = reinterpret_cast<const uint16_t*>(B_sf + (size_t)n1 * (K >> 4));
-        float acc0[M], acc1[M];
+    float acc[R][M];
 #pragma unroll
-        for (int m = 0; m < M; ++m) acc0[m] = acc1[m] = 0.f;
-        // batches of kGemvBatch chunks per lane and row: all loads of a batch
-        // are issued before any of its arithmetic
-        for (int cb = lane; cb < chunks; cb += 32 * kGemvBatch) {
-            uint4 q0[kGemvBatch], q1[kGemvBatch];
-            uint32_t t0[kGemvBatch], t1[kGemvBatch];
+    for (int r = 0; r < R; ++r)
 #pragma unroll
-            for (int u = 0; u < kGemvBatch; ++u) {
-                const int c = cb + 32 * u;
-                if (c < chunks) {
-                    q0[u] = __ldcs(row0 + c);
-                    q1[u] = __ldcs(row1 + c);
-                    t0[u] = __ldcs(srow0 + c);
-                    t1[u] = __ldcs(srow1 + c);
-                }
-            }
+        for (int m = 0; m < M; ++m) acc[r][m] = 0.f;
+    for (int it = 0; it < items; ++it) {
+        const int k = it / nbat, bat = it - k * nbat;
+        const int n0 = R * (wid + k * warps);
+        const int c0 = lane + 32 * kGemvBatch * bat;
+        if (it + 1 < items) {
+            const int k1 = (it + 1) / nbat, bat1 = (it + 1) - k1 * nbat;
+            gemv_load<R>(nxt, B, B_sf, R * (wid + k1 * warps), N, K, lane + 32 * kGemvBatch * bat1, chunks);
+        }
 #pragma unroll
-            for (int u = 0; u < kGemvBatch; ++u) {
-                const int c = cb + 32 * u;
-                if (c < chunks) {
-                    const float s00 = e4m3_to_float(t0[u] & 0xFFu), s01 = e4m3_to_float(t0[u] >> 8);
-                    const float s10 = e4m3_to_float(t1[u] & 0xFFu), s11 = e4m3_to_float(t1[u] >> 8);
+        for (int u = 0; u < kGemvBatch; ++u) {
+            const int c = c0 + 32 * u;
+            if (c < chunks) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float s0 = e4m3_to_float(cur.t[u][r] & 0xFFu), s1 = e4m3_to_float(cur.t[u][r] >> 8);
 #pragma unroll
                     for (int m = 0; m < M; ++m) {
-                        const float* xk = xs + (m * chunks + c) * kGemvRow;
-                        acc0[m] = fmaf(block16(q0[u].x, q0[u].y, xk), s00, acc0[m]);
-                        acc0[m] = fmaf(block16(q0[u].z, q0[u].w, xk + 16), s01, acc0[m]);
-                        acc1[m] = fmaf(block16(q1[u].x, q1[u].y, xk), s10, acc1[m]);
-                        acc1[m] = fmaf(block16(q1[u].z, q1[u].w, xk + 16), s11, acc1[m]);
+                        const uint4* xk = reinterpret_cast<const uint4*>(
+                            gemv_smem + ((size_t)m * chunks + c) * kGemvRowBytes);
+                        const float2 f = *reinterpret_cast<const float2*>(xf + (size_t)m * (K >> 4) + 2 * c);
+                        acc[r][m] = fmaf(block16(cur.q[u][r].x, cur.q[u][r].y, xk), s0 * f.x, acc[r][m]);
+                        acc[r][m] = fmaf(block16(cur.q[u][r].z, cur.q[u][r].w, xk + 2), s1 * f.y, acc[r][m]);
                     }
                 }
             }
         }
+        if (bat == nbat - 1) {   // the row group is complete
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-            float v0 = acc0[m], v1 = acc1[m];
+            for (int r = 0; r < R; ++r) {
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                v0 += __shfl_xor_sync(0xffffffffu, v0, o);
-                v1 += __shfl_xor_sync(0xffffffffu, v1, o);
-            }
-            if (lane == 0) {
-                y[(size_t)m * N + n0] = __float2bfloat16_rn(al * v0);
-                if (two) y[(size_t)m * N + n1] = __float2bfloat16_rn(al * v1);
+                for (int m = 0; m < M; ++m) {
+                    float v = acc[r][m];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                    if (lane == 0 && n0 + r < N) y[(size_t)m * N + n0 + r] = __float2bfloat16_rn(al * v);
+                    acc[r][m] = 0.f;
+                }
             }
         }
+        cur = nxt;
     }
 }
 

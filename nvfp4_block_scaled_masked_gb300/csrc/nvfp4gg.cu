@@ -416,8 +416,9 @@ namespace {
 template <int M>
 int launch_gemv(DeviceState* d, const void* x, const void* B, const void* B_sf, const float* alpha,
                 void* y, int N, int K, cudaStream_t st) {
-    auto kern = gemv_w4a16_kernel<M>;
-    const int smem = M * (K / 32) * kGemvRow * (int)sizeof(float);
+    constexpr int R = M <= 4 ? 2 : 1;   // weight rows per warp (register budget, grid balance)
+    auto kern = gemv_w4a16_kernel<M, R>;
+    const int smem = (int)gemv_smem_bytes(M, K);
     static bool attr_done[kMaxDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4GG_ERR_CUDA;
@@ -427,13 +428,13 @@ int launch_gemv(DeviceState* d, const void* x, const void* B, const void* B_sf, 
             return NVFP4GG_ERR_CUDA;
         attr_done[dev] = true;
     }
-    // as many CTAs per SM as registers and the staged tokens allow (more
-    // warps, more loads in flight), row pairs grid-strided over all warps
+    // as many CTAs per SM as registers and the staged tokens allow, groups of
+    // R rows grid-strided over all warps
     int per_sm = 1;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kGemvThreads, smem) !=
             cudaSuccess || per_sm < 1)
         per_sm = 1;
-    const long long need = (((long long)N + 1) / 2 * 32 + kGemvThreads - 1) / kGemvThreads;
+    const long long need = (((long long)N + R - 1) / R * 32 + kGemvThreads - 1) / kGemvThreads;
     long long grid = (long long)per_sm * d->sms;
     if (grid > need) grid = need;
     kern<<<(int)grid, kGemvThreads, smem, st>>>(
@@ -450,7 +451,7 @@ int nvfp4_gemv_w4a16(const void* x, const void* B, const void* B_sf, const float
                      int M, int N, int K, void* stream) {
     if (!x || !B || !B_sf || !alpha || !y) return NVFP4GG_ERR_NULL;
     if (M < 1 || M > kGemvMaxTokens || N < 1 || N > (1 << 24) || K < 32 || K % 32 != 0 ||
-        (long long)M * (K / 32) * kGemvRow * 4 > kGemvMaxSmem)
+        gemv_smem_bytes(M, K) > kGemvMaxSmem)
         return NVFP4GG_ERR_SHAPE;
     if (!aligned(x, 16) || !aligned(B, 16) || !aligned(B_sf, 2) || !aligned(y, 2) ||
         !aligned(alpha, 4))

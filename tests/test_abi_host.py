@@ -205,8 +205,10 @@ def test_gemv_argument_checks(lib):
     assert f(*a) == binding.ERR_SHAPE            # M > 8
     a = list(args); a[7] = 4008
     assert f(*a) == binding.ERR_SHAPE            # K % 32 != 0
-    a = list(args); a[5] = 8; a[7] = 8192
+    a = list(args); a[5] = 8; a[7] = 8960
     assert f(*a) == binding.ERR_SHAPE            # tokens do not fit shared memory
+    a = list(args); a[5] = 1; a[7] = 71520
+    assert f(*a) == binding.ERR_SHAPE            # M * K = 71520 > 71493
     a = list(args); a[1] = FAKE + 8
     assert f(*a) == binding.ERR_ALIGN
     a = list(args); a[4] = None

@@ -59,3 +59,51 @@ def test_gemv_llama_projection_full(lib):
     _, ref = oracle.gemv_w4a16(d["x"], d["B"], d["B_sf"], d["alpha"][0], d["cfg"].K)
     vals = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
     assert oracle.tolerance_ok(vals, ref, np.abs(ref).max()).all()
+
+
+def _bf16_pattern(rng, shape, exp_lo, exp_hi):
+    """Random bf16 bit patterns: random sign, biased exponent in [exp_lo,
+    exp_hi] (0 = subnormal or zero), random 7-bit mantissa."""
+    sign = rng.integers(0, 2, shape).astype(np.uint16)
+    exp = rng.integers(exp_lo, exp_hi + 1, shape).astype(np.uint16)
+    man = rng.integers(0, 128, shape).astype(np.uint16)
+    return (sign << 15) | (exp << 7) | man
+
+
+def test_gemv_activation_range(lib):
+    """Activations over bf16's whole finite range, one token per kind, each
+    token checked against its own largest output: zero blocks between normal
+    ones, subnormal and near-subnormal values, values near 1e30, and blocks
+    mixing 2^-40 .. 2^10 (the staging's per-block factor at its limits)."""
+    M, N, K = 5, 300, 2048
+    cfg = W.Config("v0", f"gemv {M}x{N}x{K}", 1, M, N, K, "fixed", masked_list=(M,),
+                   kind="gemv_w4a16")
+    d = W.generate_gemv(cfg, seed=77)
+    rng = np.random.default_rng(78)
+    x = np.empty((M, K), np.uint16)
+    x[0] = _bf16_pattern(rng, K, 120, 130)
+    x[0].reshape(-1, 16)[::3] = 0                       # every third block all zero
+    x[1] = _bf16_pattern(rng, K, 0, 0)                  # subnormal (and some zeros)
+    x[2] = _bf16_pattern(rng, K, 0, 3)                  # straddles the normal boundary
+    x[3] = _bf16_pattern(rng, K, 215, 226)              # about 1e28 .. 1e31
+    x[4] = _bf16_pattern(rng, K, 127 - 40, 127 + 10)    # 50 binades inside each block
+    d["x"] = x
+    y = run(lib, d)
+    _, ref = oracle.gemv_w4a16(x, d["B"], d["B_sf"], d["alpha"][0], K)
+    vals = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    for m in range(M):
+        ok = oracle.tolerance_ok(vals[m], ref[m], np.abs(ref[m]).max())
+        assert ok.all(), f"token {m}: {(~ok).sum()} of {N} outside tolerance"
+
+
+@pytest.mark.parametrize("M,K", [(8, 8928), (1, 71488)])
+def test_gemv_largest_staging(lib, M, K):
+    """The largest token staging shared memory takes (M * K <= 71493)."""
+    N = 97
+    cfg = W.Config("v0", f"gemv {M}x{N}x{K}", 1, M, N, K, "fixed", masked_list=(M,),
+                   kind="gemv_w4a16")
+    d = W.generate_gemv(cfg, seed=M + K)
+    y = run(lib, d)
+    _, ref = oracle.gemv_w4a16(d["x"], d["B"], d["B_sf"], d["alpha"][0], K)
+    vals = (y.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    assert oracle.tolerance_ok(vals, ref, np.abs(ref).max()).all()
