@@ -40,7 +40,8 @@ def run(lib, d):
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 256, 512), (3, 1000, 2048), (8, 130, 4096), (1, 37, 32),
-                                   (2, 4096, 14336)])
+                                   (2, 4096, 14336), (1, 7, 256), (4, 5000, 1024), (5, 153, 768),
+                                   (1, 151, 2304)])
 def test_gemv_matches_oracle(lib, M, N, K):
     cfg = W.Config("v0", f"gemv {M}x{N}x{K}", 1, M, N, K, "fixed", masked_list=(M,),
                    kind="gemv_w4a16")
