@@ -52,24 +52,31 @@ def load_peaks():
         return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
 
 
-def kernel_source_hash() -> str:
+# Sources each kernel family is compiled from: a change to any of them makes
+# that family's recorded traffic stale.
+KERNEL_SOURCES = {
+    "gemm": ("ptx.cuh", "gemm.cuh", "gemm_pair.cuh", "nvfp4gg.cu"),
+    "gemv": ("gemv.cuh", "nvfp4gg.cu"),
+}
+
+
+def kernel_source_hash(family: str = "gemm") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "nvfp4_block_scaled_masked_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(f.read())
+    for name in KERNEL_SOURCES[family]:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(config_key: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel source for this workload; else None."""
+    on the current source of the workload's kernel family; else None."""
     try:
         text = open(PROFILE_TRAFFIC).read()
     except OSError:
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash("gemv" if W.lookup(config_key).kind == "gemv_w4a16" else "gemm")
     for line in text.splitlines():
         m = re.match(r"\s*(\w+)\s+source=(\w+)\s+dram_bytes_per_launch=(\d+)", line)
         if m and m.group(1) == config_key and m.group(2) == src:
