@@ -15,6 +15,8 @@ Two implementations live here, written independently of each other:
 * ``swiglu`` applies the MoE block's SwiGLU step to GEMM1's unrounded fp64
   output (``silu(gate) * up``, one bf16 rounding), for the fused GEMM1
   epilogue.
+* ``quantize_nvfp4`` encodes bf16 activations as NVFP4 for GEMM2's A
+  (float32 steps, each rounded as IEEE prescribes; see its docstring).
 
 The operation is the one the page "The CuteDSL Gamble: Chasing Kernel
 Efficiency on Blackwell GPUs" describes for FlashInfer's
@@ -270,6 +272,76 @@ def swiglu(ref64, masked_m, C_init_half):
         out[g, :m] = y
         C[g, :m] = bf16_bits_any(y)
     return C, out
+
+
+# Non-negative finite e4m3 values, byte 0x00 .. 0x7E in increasing order.
+_E4M3_POS = E4M3_TABLE[:127].copy()
+
+
+def _round_to_grid(v, grid):
+    """Index of the nearest grid point to each v >= 0 (grid ascending, exact
+    in fp64; v float32 or fp64), ties to the even index, values beyond the
+    last point to the last (saturation)."""
+    v = np.asarray(v, dtype=np.float64)
+    hi = np.clip(np.searchsorted(grid, v, side="left"), 0, len(grid) - 1)
+    lo = np.clip(hi - 1, 0, len(grid) - 1)
+    d_lo = v - grid[lo]
+    d_hi = grid[hi] - v
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    idx = np.where(pick_hi, hi, lo)
+    return np.where(v >= grid[-1], len(grid) - 1, idx)
+
+
+def e4m3_encode(s):
+    """e4m3 byte of each s >= 0 (float32): round to nearest, ties to even
+    (the even byte: its low bit is the mantissa's), saturating at 448."""
+    return _round_to_grid(s, _E4M3_POS).astype(np.uint8)
+
+
+def e2m1_encode(w):
+    """e2m1 code of each w (float32): |w| to the nearest of 0, 0.5, 1, 1.5,
+    2, 3, 4, 6 (ties to the even code), saturating at 6; the sign bit for
+    negative non-zero results; a zero result is +0 (code 0)."""
+    w = np.asarray(w, dtype=np.float64)
+    mag = _round_to_grid(np.abs(w), _E2M1_MAG).astype(np.uint8)
+    neg = (w < 0) & (mag > 0)
+    return (mag | (neg.astype(np.uint8) << 3)).astype(np.uint8)
+
+
+def quantize_nvfp4(x_bits, qscale):
+    """NVFP4 encoding of bf16 activations (bits uint16 [R, L], L % 16 == 0)
+    with one float32 pre-scale per row (qscale [R]), for GEMM2's A after the
+    MoE block's SwiGLU step (page "LLM-Assisted Kernel Development in CuTe
+    DSL, Gluon, Helion and Triton", mixture-of-experts section: GEMM1,
+    SwiGLU, GEMM2 per expert).  The pages give no quantisation recipe;
+    reading (the NVFP4 format used everywhere here, scale chosen so that the
+    block's largest magnitude meets the largest code), per 16-element block,
+    every step in float32 with IEEE round-to-nearest-even:
+      z_i   = x_i * q                  (x widened to float32 exactly)
+      amax  = max_i |z_i|
+      sf    = e4m3(amax / 6)           (e4m3_encode: nearest, saturating)
+      d     = the value of sf
+      code_i = e2m1(z_i / d) if d > 0 else 0   (e2m1_encode)
+    So x_i ~ code_i * d / q; GEMM2's alpha carries the 1/q.  Returns (codes
+    uint8 [R, L/2], low nibble = even element; sf uint8 [R, L/16])."""
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    R, L = x_bits.shape
+    assert L % 16 == 0
+    x = (x_bits.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    q = np.asarray(qscale, dtype=np.float32).reshape(R, 1)
+    z = (x * q).astype(np.float32)                       # float32 products
+    assert np.all(np.isfinite(z)), "finite activations only"
+    zb = z.reshape(R, L // 16, 16)
+    amax = np.abs(zb).max(axis=-1)
+    s = (amax / np.float32(6.0)).astype(np.float32)      # float32 quotient
+    sf = e4m3_encode(s)
+    d = E4M3_TABLE[sf].astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        w = (zb / d[..., None]).astype(np.float32)
+    w = np.where(d[..., None] > 0, w, np.float32(0.0))
+    codes = e2m1_encode(w).reshape(R, L)
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, sf.reshape(R, L // 16)
 
 
 def gemv_w4a16(x_bits, B, B_sf, alpha, K):

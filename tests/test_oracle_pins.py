@@ -442,3 +442,122 @@ def test_gemv_integer_case_is_int64_matmul():
     x = torch.from_numpy(xi.astype(np.float32)).to(torch.bfloat16).view(torch.int16).numpy().astype(np.uint16)
     _, y = oracle.gemv_w4a16(x, B, B_sf, 1.0, K)
     np.testing.assert_array_equal(y, (xi.astype(np.int64) @ vals[ib].T).astype(np.float64))
+
+
+# ---------------------------------------------------------------- NVFP4 quantiser
+
+def _bf16_bits_exact(v):
+    """bf16 bits of float32 values that bf16 holds exactly (asserted)."""
+    f = np.asarray(v, dtype=np.float32)
+    b = f.view(np.uint32)
+    assert np.all((b & 0xFFFF) == 0), "value not exact in bf16"
+    return (b >> 16).astype(np.uint16)
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    """Round to nearest even on the e4m3 grid, checked against torch's
+    float32 -> float8_e4m3fn conversion for values within [0, 448]."""
+    rng = np.random.default_rng(5)
+    s = np.concatenate([rng.uniform(0, 448, 20000), 2.0 ** rng.uniform(-12, 8.8, 20000),
+                        oracle._E4M3_POS[:-1] + np.diff(oracle._E4M3_POS) / 2]).astype(np.float32)
+    s = s[s <= 448]
+    ref = torch.from_numpy(s).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_encode(s), ref)
+
+
+def test_e4m3_encode_ties_and_saturation():
+    cases = {1.0625: 0x38, 1.1875: 0x3A, 2.0 ** -10: 0x00, 3 * 2.0 ** -10: 0x02, 448.0: 0x7E,
+             463.0: 0x7E, 500.0: 0x7E, 1e30: 0x7E, 0.0: 0x00}
+    got = oracle.e4m3_encode(np.float32(list(cases)))
+    assert list(got) == list(cases.values())
+
+
+def test_e2m1_encode_ties_signs_saturation():
+    # midpoints go to the even code: 0.25 -> 0, 0.75 -> 1.0, 1.25 -> 1.0,
+    # 1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4; beyond 6 saturates; -0 is +0
+    w = np.float32([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, 6.5, 1e9, -0.25, -0.3, -5.0, -7.0, 0.0, -0.0])
+    want = [0, 2, 2, 4, 4, 6, 6, 7, 7, 0, 9, 14, 15, 0, 0]
+    assert list(oracle.e2m1_encode(w)) == want
+
+
+def _exact_blocks(rng, R, L, sf_lo=0x01, sf_hi=0x70):
+    """Blocks code * d with one element of every block at +-6 (so the block's
+    scale is d exactly), codes != -0, d a positive e4m3 value."""
+    codes = rng.integers(0, 15, (R, L)).astype(np.uint8)
+    codes[codes >= 8] += 1                             # skip 0x8 (-0)
+    blk = codes.reshape(R, L // 16, 16)
+    pos = rng.integers(0, 16, (R, L // 16))
+    sign = rng.integers(0, 2, (R, L // 16)).astype(np.uint8) << 3
+    np.put_along_axis(blk, pos[..., None], (7 | sign)[..., None], axis=-1)
+    sf = rng.integers(sf_lo, sf_hi + 1, (R, L // 16)).astype(np.uint8)
+    vals = oracle.E2M1_TABLE[codes] * np.repeat(oracle.E4M3_TABLE[sf], 16, axis=-1)
+    return codes, sf, _bf16_bits_exact(vals.astype(np.float32))
+
+
+def test_quantize_round_trips_exact_blocks():
+    """Encoding values that are exactly code * d, with the block maximum at
+    6 d, returns those codes and d's byte (subnormal scales included); this
+    fixes the block grouping, the nibble order and the code table."""
+    rng = np.random.default_rng(11)
+    codes, sf, x = _exact_blocks(rng, 7, 256)
+    got_c, got_sf = oracle.quantize_nvfp4(x, np.ones(7, np.float32))
+    np.testing.assert_array_equal(got_sf, sf)
+    np.testing.assert_array_equal(got_c, (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8))
+
+
+def test_quantize_midpoints_round_to_even_codes():
+    d = 0.5                                            # byte 0x30
+    m = [6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -2.5, -5.0, 4.0, -6.0, 0.0, 1.0]
+    want = [7, 0, 2, 2, 4, 4, 6, 6, 0, 10, 12, 14, 6, 15, 0, 2]
+    x = _bf16_bits_exact(np.float32(m) * np.float32(d))[None, :]
+    c, sf = oracle.quantize_nvfp4(x, np.ones(1, np.float32))
+    assert sf[0, 0] == 0x30
+    got = [int(c[0, j // 2] >> (4 * (j & 1)) & 15) for j in range(16)]
+    assert got == want
+
+
+def test_quantize_prescale_power_of_two_shifts_the_scale_byte():
+    """q -> 2^j q leaves the codes and moves the scale byte by 8 j (one e4m3
+    exponent step per factor 2) while the scale stays normal and unsaturated."""
+    rng = np.random.default_rng(12)
+    _, _, x = _exact_blocks(rng, 3, 64, sf_lo=0x30, sf_hi=0x48)
+    c0, s0 = oracle.quantize_nvfp4(x, np.ones(3, np.float32))
+    for j in (-2, 1, 3):
+        c, s = oracle.quantize_nvfp4(x, np.full(3, 2.0 ** j, np.float32))
+        np.testing.assert_array_equal(c, c0)
+        np.testing.assert_array_equal(s.astype(int), s0.astype(int) + 8 * j)
+
+
+def test_quantize_zero_tiny_and_saturating_blocks():
+    x = np.zeros((1, 48), np.uint16)
+    x[0, 16:32] = _bf16_bits_exact(np.full(16, 2.0 ** -20, np.float32))     # amax / 6 < 2^-10
+    blk = np.full(16, 1.0, np.float32)
+    blk[3] = 6.25                                      # amax / 6 = 1.04 -> scale 1.0, w = 6.25 -> 6
+    x[0, 32:] = _bf16_bits_exact(blk)
+    c, sf = oracle.quantize_nvfp4(x, np.ones(1, np.float32))
+    assert list(sf[0]) == [0, 0, 0x38]
+    assert np.all(c[0, :16] == 0)
+    third = [int(c[0, 16 + j // 2] >> (4 * (j & 1)) & 15) for j in range(16)]
+    assert third == [2, 2, 2, 7] + [2] * 12
+
+
+def test_quantize_error_bound():
+    """Every decoded element lies within half a grid step of z = x q: at
+    most d / 4 where |z| <= 2 d, at most d elsewhere (steps 0.5, 1, 2 times d;
+    saturation adds at most 0.375 d, covered by the second bound since
+    amax / d <= 6 * (1 + 1/16))."""
+    rng = np.random.default_rng(13)
+    R, L = 9, 512
+    sign = rng.integers(0, 2, (R, L)).astype(np.uint16)
+    exp = rng.integers(120, 135, (R, L)).astype(np.uint16)          # 2^-7 .. 2^8
+    x = (sign << 15) | (exp << 7) | rng.integers(0, 128, (R, L)).astype(np.uint16)
+    q = np.float32(2.0) ** rng.integers(-6, 3, R).astype(np.float32)   # scales stay in range
+    c, sf = oracle.quantize_nvfp4(x, q)
+    z = (x.astype(np.uint32) << 16).view(np.float32).astype(np.float64) * q[:, None].astype(np.float64)
+    dec = oracle.decode_numpy(c, sf, L)
+    d = np.repeat(oracle.E4M3_TABLE[sf], 16, axis=-1)
+    assert np.all(d > 0) and np.all(sf < 0x7E)
+    err = np.abs(dec - z)
+    small = np.abs(z) <= 2 * d
+    assert np.all(err[small] <= d[small] / 4 * (1 + 1e-6))
+    assert np.all(err <= d * (1 + 1e-6))
