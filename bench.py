@@ -257,6 +257,9 @@ def main():
                     help="time nvfp4_grouped_gemm_nt_masked_splitk with this split (0 = automatic)")
     ap.add_argument("--swiglu", action="store_true",
                     help="time the fused GEMM1 + SwiGLU entry point (output N/2 columns)")
+    ap.add_argument("--swiglu-quant", action="store_true",
+                    help="time the fused GEMM1 + SwiGLU entry point that also writes GEMM2's "
+                         "NVFP4 activations (codes + scales of the N/2 columns)")
     ap.add_argument("--pair-mode", default="auto", choices=["auto", "on", "off"],
                     help="prefill kernel family: CTA pairs (on), single CTAs (off), or the "
                          "library's automatic choice")
@@ -294,9 +297,15 @@ def main():
 
     d = W.generate(cfg)
     counts = W.algorithmic_counts(cfg, d["masked_m"])
+    if args.swiglu_quant:
+        args.swiglu = True
     if args.swiglu:   # the fused epilogue writes N/2 bf16 columns per valid row
         counts["bytes"] -= counts["out_bytes"] // 2
         counts["out_bytes"] //= 2
+    if args.swiglu_quant:   # + N/2 e2m1 codes and N/32 e4m3 scales per valid row
+        q_bytes = counts["rows"] * (cfg.N // 4 + cfg.N // 32)
+        counts["bytes"] += q_bytes
+        counts["out_bytes"] += q_bytes
     stream = torch.cuda.current_stream()
 
     # one-time weight re-layout, timed separately (median of 5)
@@ -324,6 +333,16 @@ def main():
             binding.nvfp4_grouped_gemm_nt_masked_splitk(
                 prob.A, prob.A_sf, prob.B_prep, prob.B_sf_prep, prob.alpha, prob.masked_m, prob.C,
                 cfg.G, cfg.M_max, cfg.N, cfg.K, args.splitk, splitk_ws, splitk_bytes)
+    elif args.swiglu_quant:
+        C_half = torch.empty((cfg.G, cfg.M_max, cfg.N // 2), dtype=torch.int16, device="cuda")
+        A2 = torch.empty((cfg.G, cfg.M_max, cfg.N // 4), dtype=torch.uint8, device="cuda")
+        A2_sf = torch.empty((cfg.G, cfg.M_max, cfg.N // 32), dtype=torch.uint8, device="cuda")
+        qscale = torch.full((cfg.G,), 2.0 ** -9, dtype=torch.float32, device="cuda")
+
+        def run_step():
+            binding.nvfp4_grouped_gemm_nt_masked_swiglu_quant(
+                prob.A, prob.A_sf, prob.B_prep, prob.B_sf_prep, prob.alpha, prob.masked_m, C_half,
+                qscale, A2, A2_sf, cfg.G, cfg.M_max, cfg.N, cfg.K)
     elif args.swiglu:
         C_half = torch.empty((cfg.G, cfg.M_max, cfg.N // 2), dtype=torch.int16, device="cuda")
 
@@ -409,7 +428,8 @@ def main():
         "prepare_weights_ms": statistics.median(prep_ms),
         "gpu_launches": args.steps,
         "entry_point": ("nvfp4_grouped_gemm_nt_masked_splitk(split_k=%d)" % args.splitk
-                        if args.splitk >= 0 else "nvfp4_grouped_gemm_nt_masked_swiglu"
+                        if args.splitk >= 0 else "nvfp4_grouped_gemm_nt_masked_swiglu_quant"
+                        if args.swiglu_quant else "nvfp4_grouped_gemm_nt_masked_swiglu"
                         if args.swiglu else "nvfp4_grouped_gemm_nt_masked"),
         "pair_mode": args.pair_mode,
         "wall_s_timed_region": wall,

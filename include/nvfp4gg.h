@@ -265,6 +265,47 @@ int nvfp4_grouped_gemm_nt_masked_swiglu(const void* A, const void* A_sf, const v
                                         void* C, int G, int M_max, int N, int K, void* stream);
 
 /*
+ * NVFP4 encoding of bf16 activations, GEMM2's A after the SwiGLU step (the
+ * MoE expert block of the page "LLM-Assisted Kernel Development in CuTe DSL,
+ * Gluon, Helion and Triton" runs GEMM1, SwiGLU, GEMM2 per expert; the pages
+ * give no quantisation recipe, so this is the reading).  Per 16-element
+ * block of a row, in fp32 with round-to-nearest-even:
+ *     z_i = x_i * q;  sf = e4m3(max|z_i| / 6) (saturating at 448);
+ *     d = value(sf);  code_i = e2m1(z_i / d) (saturating at 6), 0 if d == 0
+ * so x_i ~ code_i * d / q: a GEMM2 on these codes takes alpha / q.  Zero
+ * codes are written as +0.
+ *   x        device bf16 [R][L] row-major, 16-byte aligned, finite
+ *   qscale   device f32; row r uses qscale[r / rows_per_scale]
+ *            (rows_per_scale = R: one per tensor; = M_max: one per expert)
+ *   codes    device u8 [R][L/2] (low nibble = even element), 8-byte aligned
+ *   sf       device u8 [R][L/16]
+ * Limits: R >= 1, L % 16 == 0, R * L <= 2^40.  The layouts match A and
+ * A_sf of nvfp4_grouped_gemm_nt_masked (K = L).
+ */
+int nvfp4_quantize_bf16(const void* x, const float* qscale, void* codes, void* sf, int R, int L,
+                        int rows_per_scale, void* stream);
+
+/*
+ * nvfp4_grouped_gemm_nt_masked_swiglu whose epilogue also encodes its bf16
+ * output as NVFP4 for GEMM2, by the recipe of nvfp4_quantize_bf16 with one
+ * pre-scale per expert: the codes are those nvfp4_quantize_bf16 gives for
+ * the bf16 values C holds (rows_per_scale = M_max).
+ *   C        bf16 [G][M_max][N/2] as in the SwiGLU entry, or NULL (then only
+ *            the NVFP4 output is written)
+ *   qscale   device f32 [G], expert g's pre-scale
+ *   A2       device u8 [G][M_max][N/4], 16-byte aligned: GEMM2's A codes
+ *   A2_sf    device u8 [G][M_max][N/32]: GEMM2's A_sf
+ * Rows m >= masked_m[g] of C, A2 and A2_sf are never written.  GEMM2 is then
+ * nvfp4_grouped_gemm_nt_masked(A2, A2_sf, W2 prepared, ..., K = N/2) with
+ * alpha2[g] / qscale[g].  Other arguments and limits as in the SwiGLU entry.
+ */
+int nvfp4_grouped_gemm_nt_masked_swiglu_quant(const void* A, const void* A_sf, const void* B,
+                                              const void* B_sf, const float* alpha,
+                                              const int* masked_m, void* C, const float* qscale,
+                                              void* A2, void* A2_sf, int G, int M_max, int N, int K,
+                                              void* stream);
+
+/*
  * End-to-end variant for callers whose activations live in host memory.
  *   h_A, h_A_sf, h_alpha, h_masked_m: HOST buffers laid out as above (pinned
  *       memory gives asynchronous copies)

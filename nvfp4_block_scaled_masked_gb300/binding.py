@@ -38,6 +38,8 @@ EXPORTS = (
     "nvfp4_grouped_gemm_nt_masked_signals",
     "nvfp4_prepare_weights_swiglu",
     "nvfp4_grouped_gemm_nt_masked_swiglu",
+    "nvfp4_grouped_gemm_nt_masked_swiglu_quant",
+    "nvfp4_quantize_bf16",
     "nvfp4_host_staging_bytes",
     "nvfp4_grouped_gemm_nt_masked_host",
     "nvfp4_gg_set_sm_count",
@@ -92,6 +94,10 @@ def load():
     lib.nvfp4_prepare_weights_swiglu.restype = i
     lib.nvfp4_grouped_gemm_nt_masked_swiglu.argtypes = [vp] * 7 + [i] * 4 + [vp]
     lib.nvfp4_grouped_gemm_nt_masked_swiglu.restype = i
+    lib.nvfp4_grouped_gemm_nt_masked_swiglu_quant.argtypes = [vp] * 10 + [i] * 4 + [vp]
+    lib.nvfp4_grouped_gemm_nt_masked_swiglu_quant.restype = i
+    lib.nvfp4_quantize_bf16.argtypes = [vp] * 4 + [i] * 3 + [vp]
+    lib.nvfp4_quantize_bf16.restype = i
     lib.nvfp4_host_staging_bytes.argtypes = [i] * 4
     lib.nvfp4_host_staging_bytes.restype = sz
     lib.nvfp4_grouped_gemm_nt_masked_host.argtypes = [vp] * 7 + [i] * 4 + [vp, sz, vp]
@@ -207,6 +213,23 @@ def nvfp4_grouped_gemm_nt_masked_swiglu(A, A_sf, B, B_sf, alpha, masked_m, C, G,
                                                       _ptr(alpha), _ptr(masked_m), _ptr(C),
                                                       G, M_max, N, K, _stream(stream)),
            "nvfp4_grouped_gemm_nt_masked_swiglu")
+
+
+def nvfp4_grouped_gemm_nt_masked_swiglu_quant(A, A_sf, B, B_sf, alpha, masked_m, C, qscale, A2,
+                                              A2_sf, G, M_max, N, K, stream=None):
+    """SwiGLU GEMM1 whose epilogue also writes GEMM2's NVFP4 A (A2, A2_sf);
+    C may be None."""
+    _check(load().nvfp4_grouped_gemm_nt_masked_swiglu_quant(
+        _ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf), _ptr(alpha), _ptr(masked_m), _ptr(C),
+        _ptr(qscale), _ptr(A2), _ptr(A2_sf), G, M_max, N, K, _stream(stream)),
+        "nvfp4_grouped_gemm_nt_masked_swiglu_quant")
+
+
+def nvfp4_quantize_bf16(x, qscale, codes, sf, R, L, rows_per_scale, stream=None):
+    """NVFP4 encoding of bf16 rows x [R][L] (qscale[r // rows_per_scale])."""
+    _check(load().nvfp4_quantize_bf16(_ptr(x), _ptr(qscale), _ptr(codes), _ptr(sf), R, L,
+                                      rows_per_scale, _stream(stream)),
+           "nvfp4_quantize_bf16")
 
 
 def nvfp4_splitk_workspace_bytes(G, M_max, N, K, split_k=0) -> int:

@@ -48,6 +48,7 @@
 #pragma once
 #include <cuda_bf16.h>
 #include "ptx.cuh"
+#include "quant.cuh"
 #include "nvfp4gg.h"
 
 namespace nvfp4gg {
@@ -84,6 +85,12 @@ struct GemmParams {
     // in all; token tensor maps are over [M_total] rows with one group
     int contiguous;
     int M_total;
+    // SwiGLU epilogue only: also encode the bf16 output as NVFP4 for GEMM2
+    // (qa non-null): codes qa [G][M_max][N/4], scales qsf [G][M_max][N/32],
+    // expert g pre-scaled by qscale[g]; C may then be null (no bf16 store)
+    uint8_t* qa;
+    uint8_t* qsf;
+    const float* qscale;
 };
 
 // Row of C holding token `tok` of expert g: g * M_max + tok in the masked
@@ -572,6 +579,12 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                 // [16 tokens][16 columns] bf16, stored by 32 lanes x 16 bytes
                 const int NO = p.N >> 1;
                 const int oc0 = tc.nt * 64 + quad * 16;
+                // NVFP4 output: this warp's 16 columns are one 16-element
+                // block of GEMM2's K, i.e. token t's block is row t of the
+                // staged bf16 tile; lane t < 16 encodes it after the tile
+                // is staged
+                const bool quant = p.qa != nullptr;
+                const float qs = quant ? __ldg(p.qscale + tc.g) : 0.f;
 #pragma unroll 1
                 for (int c = 0; c < TT_MAX / 16; ++c) {
                     if (c * 16 >= tc.w) break;
@@ -590,8 +603,19 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                     const int tok = tc.t0 + c * 16 + t;
                     const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + t * 32 + hh * 16);
                     const long long row = out_row(p, off, tc.g, tok);
-                    if (tok < t_end && oc0 < NO && row >= 0)
+                    if (p.C && tok < t_end && oc0 < NO && row >= 0)
                         *reinterpret_cast<uint4*>(p.C + row * NO + oc0 + 8 * hh) = v;
+                    if (quant && lane < 16) {
+                        const int qtok = tc.t0 + c * 16 + lane;
+                        const long long qrow = out_row(p, off, tc.g, qtok);
+                        if (qtok < t_end && oc0 < NO && qrow >= 0) {
+                            const uint4* src = reinterpret_cast<const uint4*>(stage_buf + lane * 32);
+                            uint2 qc;
+                            const uint32_t qsb = nvfp4_quant_block16(src[0], src[1], qs, qc);
+                            *reinterpret_cast<uint2*>(p.qa + qrow * (NO >> 1) + (oc0 >> 1)) = qc;
+                            p.qsf[qrow * (NO >> 4) + (oc0 >> 4)] = static_cast<uint8_t>(qsb);
+                        }
+                    }
                     __syncwarp();
                 }
                 tc_fence_before();

@@ -336,12 +336,16 @@ int auto_split(DeviceState* d, long long tiles, int K) {
 int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf, const float* alpha,
                 const int* masked_m, void* C, int G, int M_max, int N, int K, int split,
                 float* ws_part, int* ws_cnt, void* stream, bool swiglu = false,
-                int* signals = nullptr, int M_total = 0) {
-    if (!A || !A_sf || !B || !B_sf || !alpha || !masked_m || !C) return NVFP4GG_ERR_NULL;
+                int* signals = nullptr, int M_total = 0, uint8_t* qa = nullptr,
+                uint8_t* qsf = nullptr, const float* qscale = nullptr) {
+    // with the NVFP4 output of the SwiGLU epilogue (qa), C may be null
+    if (!A || !A_sf || !B || !B_sf || !alpha || !masked_m || (!C && !qa)) return NVFP4GG_ERR_NULL;
+    if (qa && (!qsf || !qscale)) return NVFP4GG_ERR_NULL;
     int rc = check_gemm_shape(G, M_max, N, K);
     if (rc != NVFP4GG_OK) return rc;
     if (!aligned(A, 16) || !aligned(A_sf, 16) || !aligned(B, 16) || !aligned(B_sf, 16) ||
-        !aligned(C, 16) || !aligned(alpha, 4) || !aligned(masked_m, 4))
+        !aligned(C, 16) || !aligned(alpha, 4) || !aligned(masked_m, 4) || !aligned(qa, 16) ||
+        !aligned(qscale, 4))
         return NVFP4GG_ERR_ALIGN;
     DeviceState* d = nullptr;
     if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
@@ -358,6 +362,9 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
         return rc;
     p.contiguous = M_total > 0 ? 1 : 0;
     p.M_total = M_total;
+    p.qa = qa;
+    p.qsf = qsf;
+    p.qscale = qscale;
     p.wq = static_cast<const uint8_t*>(B);
     p.wsf = static_cast<const uint8_t*>(B_sf);
     p.alpha = alpha;
@@ -497,6 +504,37 @@ int nvfp4_grouped_gemm_nt_masked_swiglu(const void* A, const void* A_sf, const v
     if (N % 128 != 0) return NVFP4GG_ERR_SHAPE;
     return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr, nullptr,
                        stream, true);
+}
+
+int nvfp4_grouped_gemm_nt_masked_swiglu_quant(const void* A, const void* A_sf, const void* B,
+                                              const void* B_sf, const float* alpha,
+                                              const int* masked_m, void* C, const float* qscale,
+                                              void* A2, void* A2_sf, int G, int M_max, int N, int K,
+                                              void* stream) {
+    if (!A2 || !A2_sf || !qscale) return NVFP4GG_ERR_NULL;
+    if (N % 128 != 0) return NVFP4GG_ERR_SHAPE;
+    return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr, nullptr,
+                       stream, true, nullptr, 0, static_cast<uint8_t*>(A2),
+                       static_cast<uint8_t*>(A2_sf), qscale);
+}
+
+int nvfp4_quantize_bf16(const void* x, const float* qscale, void* codes, void* sf, int R, int L,
+                        int rows_per_scale, void* stream) {
+    if (!x || !qscale || !codes || !sf) return NVFP4GG_ERR_NULL;
+    if (R < 1 || L < 16 || L % 16 != 0 || rows_per_scale < 1 || (long long)R * L > (1LL << 40))
+        return NVFP4GG_ERR_SHAPE;
+    if (!aligned(x, 16) || !aligned(codes, 8) || !aligned(qscale, 4)) return NVFP4GG_ERR_ALIGN;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != NVFP4GG_OK) return rc;
+    const long long blocks = (long long)R * (L / 16);
+    long long grid = (blocks + 255) / 256;
+    const long long cap = (long long)d->sms * 8;   // grid-stride beyond 8 CTAs per SM
+    if (grid > cap) grid = cap;
+    quantize_bf16_kernel<<<(int)grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const __nv_bfloat16*>(x), qscale, static_cast<uint8_t*>(codes),
+        static_cast<uint8_t*>(sf), blocks, L, rows_per_scale);
+    return cuda_status(cudaGetLastError());
 }
 
 size_t nvfp4_splitk_workspace_bytes(int G, int M_max, int N, int K, int split_k) {

@@ -172,6 +172,38 @@ def test_swiglu_argument_checks(lib):
     assert p(None, FAKE, 2, 256, 512, FAKE + 4096, FAKE + 8192, None) == binding.ERR_NULL
 
 
+def test_swiglu_quant_argument_checks(lib):
+    f = lib.nvfp4_grouped_gemm_nt_masked_swiglu_quant
+    # A, A_sf, B, B_sf, alpha, masked_m, C, qscale, A2, A2_sf, G, M_max, N, K, stream
+    args = [FAKE] * 10 + [2, 16, 256, 512, None]
+    for k in (7, 8, 9):                           # qscale, A2, A2_sf required
+        a = list(args); a[k] = None
+        assert f(*a) == binding.ERR_NULL
+    a = list(args); a[0] = None
+    assert f(*a) == binding.ERR_NULL
+    a = list(args); a[12] = 192                   # N % 128 != 0
+    assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[8] = FAKE + 8               # A2 not 16-byte aligned
+    assert f(*a) == binding.ERR_ALIGN
+    a = list(args); a[7] = FAKE + 2               # qscale not 4-byte aligned
+    assert f(*a) == binding.ERR_ALIGN
+
+
+def test_quantize_argument_checks(lib):
+    f = lib.nvfp4_quantize_bf16
+    args = [FAKE] * 4 + [4, 256, 4, None]
+    for k in range(4):
+        a = list(args); a[k] = None
+        assert f(*a) == binding.ERR_NULL
+    for k, v in ((4, 0), (5, 8), (5, 264), (6, 0)):   # R < 1, L < 16, L % 16, rows_per_scale < 1
+        a = list(args); a[k] = v
+        assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[0] = FAKE + 8               # x not 16-byte aligned
+    assert f(*a) == binding.ERR_ALIGN
+    a = list(args); a[2] = FAKE + 4               # codes not 8-byte aligned
+    assert f(*a) == binding.ERR_ALIGN
+
+
 def test_signals_argument_checks(lib):
     f = lib.nvfp4_grouped_gemm_nt_masked_signals
     args = [FAKE] * 7 + [2, 16, 256, 512, FAKE, None]
