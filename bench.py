@@ -55,7 +55,7 @@ def load_peaks():
 # Sources each kernel family is compiled from: a change to any of them makes
 # that family's recorded traffic stale.
 KERNEL_SOURCES = {
-    "gemm": ("ptx.cuh", "gemm.cuh", "gemm_pair.cuh", "nvfp4gg.cu"),
+    "gemm": ("ptx.cuh", "quant.cuh", "gemm.cuh", "gemm_pair.cuh", "nvfp4gg.cu"),
     "gemv": ("gemv.cuh", "nvfp4gg.cu"),
 }
 
