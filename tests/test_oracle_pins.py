@@ -561,3 +561,52 @@ def test_quantize_error_bound():
     small = np.abs(z) <= 2 * d
     assert np.all(err[small] <= d[small] / 4 * (1 + 1e-6))
     assert np.all(err <= d * (1 + 1e-6))
+
+
+def _nearest_even(v: Fraction, grid):
+    """Brute force over every grid point (exact rationals): the nearest one,
+    ties to the even index, beyond the last point the last."""
+    if v >= grid[-1]:
+        return len(grid) - 1
+    best, best_d = 0, abs(v - grid[0])
+    for i, g in enumerate(grid[1:], 1):
+        d = abs(v - g)
+        if d < best_d or (d == best_d and i % 2 == 0):
+            best, best_d = i, d
+    return best
+
+
+def test_quantize_matches_scalar_rational_brute_force():
+    """A second, scalar restatement of the encoder: float32 steps with numpy
+    scalars, every grid decision by exhaustive search in exact rationals."""
+    e4 = [Fraction(float(v)) for v in oracle._E4M3_POS]
+    e2 = [Fraction(v) for v in (0, 0.5, 1, 1.5, 2, 3, 4, 6)]
+    rng = np.random.default_rng(14)
+    R, L = 4, 64
+    sign = rng.integers(0, 2, (R, L)).astype(np.uint16)
+    exp = rng.integers(100, 140, (R, L)).astype(np.uint16)
+    x = (sign << 15) | (exp << 7) | rng.integers(0, 128, (R, L)).astype(np.uint16)
+    x[1, 16:32] = 0                                        # a zero block
+    x[2, :16] = _bf16_bits_exact(np.float32([6, .25, .75, 1.25, 1.75, 2.5, 3.5, 5] * 2) * np.float32(0.125))
+    q = np.float32([1.0, 0.37, 2.0 ** -3, 3.1])
+    c, sf = oracle.quantize_nvfp4(x, q)
+    for r in range(R):
+        for b in range(L // 16):
+            z = []
+            for i in range(16):
+                xi = np.uint32(int(x[r, 16 * b + i]) << 16).view(np.float32)
+                z.append(np.float32(xi * q[r]))
+            amax = max(abs(v) for v in z)
+            s = np.float32(np.float32(amax) / np.float32(6.0))
+            sb = _nearest_even(Fraction(float(s)), e4)
+            assert sf[r, b] == sb
+            d = np.float32(float(e4[sb]))
+            for i in range(16):
+                if d > 0:
+                    w = np.float32(z[i] / d)
+                    m = _nearest_even(Fraction(abs(float(w))), e2)
+                    code = m | (8 if (w < 0 and m > 0) else 0)
+                else:
+                    code = 0
+                got = int(c[r, 8 * b + i // 2]) >> (4 * (i & 1)) & 15
+                assert got == code, (r, b, i, float(w), got, code)
