@@ -1,10 +1,14 @@
 """Benchmark of the masked, block-scaled NVFP4 grouped GEMM-NT on GB300.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--config c2] [--impl ours|reference]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--config c4] [--impl ours|reference]
 
 One step = one call of nvfp4_grouped_gemm_nt_masked over one batch of the
-synthetic workload (default: the decode GEMM1 workload, G=32 experts,
-M_max=16, masked_m ~ U{0..8}, N=4096, K=7168).  Each timed step is bracketed by
+synthetic workload (default: the largest single-GPU workload, the prefill
+GEMM2 of a 256-expert MoE layer: G=256, masked_m from top-8 routing of 4096
+tokens, M_max=256, N=7168, K=2048, 962 GFLOP and 2.6 GB per call).  The same
+run also times the other four workloads (decode GEMM1 at 32 and 256 experts,
+the compute-bound G=8 M=2048 shape and the small masked case) and reports
+them under "per_config", with sampled parity against the oracle.  Each timed step is bracketed by
 CUDA events on the launching stream; between steps L2 is flushed by writing a
 256 MB buffer and then reading it back, so the next step starts with an L2
 that holds none of its inputs and no dirty lines.  Prints one JSON line (rank 0).  Under torchrun every rank runs an
@@ -247,12 +251,85 @@ def flush_l2(buf, i):
     return buf.view(torch_int64()).sum()
 
 
+def time_steps(run_step, steps, flush, stream):
+    """Device time of `steps` calls, each after an L2 flush, CUDA events on
+    the launching stream; returns the per-step milliseconds."""
+    import torch
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush_l2(flush, i)
+        starts[i].record(stream)
+        run_step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+PER_CONFIG_KEYS = ("c1", "c2", "c3", "c4", "c5")
+
+
+def roofline_fracs(cfg, counts, ms, peaks, probe_best):
+    """Achieved rates of one call and its fractions of the HBM and NVFP4
+    tensor roofs (measured HBM copy bandwidth; the higher MMA-probe rate)."""
+    tflops = counts["flops"] / (ms / 1e3) / 1e12
+    gbs = counts["bytes"] / (ms / 1e3) / 1e9
+    return dict(tflops=tflops, gbs=gbs, frac_hbm=gbs / peaks["hbm"],
+                frac_tensor=(tflops / probe_best) if probe_best else None,
+                bound="tensor" if cfg.key == "c5" else ("launch" if cfg.key == "c1" else "hbm"))
+
+
+def per_config_block(args, peaks, probe_best, main_key, main_ms, main_d, main_C, flush, stream):
+    """Device-timed ms and roofline fractions of every workload in one run;
+    the data and C of each are kept for the sampled parity check of the
+    CPU-baseline leg."""
+    import torch
+    from nvfp4_block_scaled_masked_gb300 import binding
+    from nvfp4_block_scaled_masked_gb300.device import Problem
+    out, kept = {}, {}
+    for key in PER_CONFIG_KEYS:
+        cfg = W.CONFIGS[key]
+        if key == main_key:
+            d, C_bits, ms_list = main_d, main_C, None
+            ms = main_ms
+        else:
+            d = W.generate(cfg)
+            prob = Problem(d)
+            for _ in range(3):
+                prob.run()
+            prob.reset_C()
+            prob.run()                       # the output kept for the parity check
+            C_bits = prob.C_bits()
+            if binding.nvfp4_gg_check_error() != 0:
+                raise RuntimeError(f"device error on {key}")
+            ms_list = time_steps(prob.run, args.per_config_steps, flush, stream)
+            if binding.nvfp4_gg_check_error() != 0:
+                raise RuntimeError(f"device error on {key}")
+            ms = statistics.median(ms_list)
+            del prob
+            torch.cuda.empty_cache()
+        counts = W.algorithmic_counts(cfg, d["masked_m"])
+        r = roofline_fracs(cfg, counts, ms, peaks, probe_best)
+        out[key] = {"workload": cfg.name, "ms": ms, "TFLOP/s": r["tflops"],
+                    "algorithmic_GB/s": r["gbs"], "bound": r["bound"],
+                    "frac_of_hbm": r["frac_hbm"], "frac_of_nvfp4_probe": r["frac_tensor"],
+                    "traffic": profiled_traffic(key), "algorithmic_bytes": counts["bytes"],
+                    "flops": counts["flops"],
+                    "steps": args.steps if ms_list is None else len(ms_list),
+                    "timing": "median of steps, CUDA events, L2 flushed before each"}
+        kept[key] = (d, C_bits)
+    return out, kept
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="c2", choices=sorted(W.CONFIGS) + sorted(W.EXTRA))
+    ap.add_argument("--config", default="c4", choices=sorted(W.CONFIGS) + sorted(W.EXTRA))
+    ap.add_argument("--per-config-steps", type=int, default=30,
+                    help="timed steps per workload in the per_config block (0: no per_config)")
     ap.add_argument("--splitk", type=int, default=-1,
                     help="time nvfp4_grouped_gemm_nt_masked_splitk with this split (0 = automatic)")
     ap.add_argument("--swiglu", action="store_true",
@@ -435,20 +512,32 @@ def main():
         "wall_s_timed_region": wall,
         "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms),
     }
+    # dense NVFP4 tensor rate, measured by the library's probes (single-CTA
+    # M = 128 MMAs at N = 256 and 192, CTA-pair M = 256 MMAs at N = 256)
+    probe = {"cta1_N256": mma_peak_tflops(256), "cta1_N192": mma_peak_tflops(192),
+             "pair_N256": mma_peak_tflops(256, pair=True)}
+    probe_best = max(probe.values())
+    line["mma_probe_tflops"] = probe
     if cfg.key == "c5":
         peak = peaks["bf16"] * NOMINAL_FP4_OVER_BF16
-        probe = {n: mma_peak_tflops(n) for n in (256, 192)}
         line["roofline"] = {"bound": "tensor", "achieved": tflops / ws, "peak": peak,
                             "unit": "TFLOP/s", "frac": tflops / ws / peak,
                             "traffic": profiled_traffic(cfg.key),
                             "peak_note": f"nvfp4 = bf16 {peaks['src']} burst x {NOMINAL_FP4_OVER_BF16:g} (nominal ratio)",
-                            "mma_probe_tflops": {f"N={n}": v for n, v in probe.items()},
-                            "frac_of_probe_N256": tflops / ws / probe[256]}
+                            "frac_of_probe": tflops / ws / probe_best,
+                            "probe_note": "the higher of the library's MMA-probe rates (mma_probe_tflops)"}
     else:
         line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm"], "unit": "GB/s",
                             "frac": gbs / peaks["hbm"], "traffic": profiled_traffic(cfg.key),
                             "algorithmic_bytes": counts["bytes"],
                             "peak_note": f"HBM copy bandwidth, {peaks['src']}"}
+    kept = {}
+    if args.per_config_steps > 0 and ws == 1:
+        plain = args.splitk < 0 and not args.swiglu
+        main_key = cfg.key if (plain and cfg.key in PER_CONFIG_KEYS) else None
+        line["per_config"], kept = per_config_block(
+            args, peaks, probe_best, main_key, ms, d, prob.C_bits() if main_key else None,
+            flush, stream)
     line["e2e"] = {"value": counts["flops"] / (e2e_med / 1e3) / 1e12, "unit": UNIT,
                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                    "ms_per_step": e2e_med, "steps": args.e2e_steps,
@@ -462,6 +551,8 @@ def main():
 
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(cfg, d, prob)
+        for key, (dk, Ck) in kept.items():
+            line["per_config"][key]["parity"] = sampled_parity(dk, Ck)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -583,25 +674,50 @@ def bench_gemv(args, cfg, ws, rank, local):
         dist.destroy_process_group()
 
 
-def mma_peak_tflops(n: int, iters: int = 1 << 16) -> float:
-    """Dense NVFP4 tensor rate from the library's MMA probe: all SMs issue
-    back-to-back M=128, N=n, K=64 block-scaled MMAs; median of 5 launches."""
+def mma_peak_tflops(n: int, iters: int = 1 << 16, pair: bool = False) -> float:
+    """Dense NVFP4 tensor rate from the library's MMA probes: all SMs issue
+    back-to-back block-scaled MMAs of K=64, M=128 per CTA (pair=False) or
+    M=256 per 2-CTA cluster (pair=True), N=n; median of 5 launches."""
     import torch
     from nvfp4_block_scaled_masked_gb300 import binding
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    binding.nvfp4_gg_mma_peak_probe(iters // 16, n)
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    probe = binding.nvfp4_gg_mma_peak_probe_pair if pair else binding.nvfp4_gg_mma_peak_probe
+    probe(iters // 16, n)
     times = []
     for _ in range(5):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        binding.nvfp4_gg_mma_peak_probe(iters, n)
+        probe(iters, n)
         e1.record()
         e1.synchronize()
         times.append(e0.elapsed_time(e1) / 1e3)
     if binding.nvfp4_gg_check_error() != 0:
         raise RuntimeError("device error in the MMA probe")
-    flops = sms * iters * 4 * 2.0 * 128 * n * 64
+    flops = (sms // 2 if pair else sms) * iters * 4 * 2.0 * (256 if pair else 128) * n * 64
     return flops / statistics.median(times) / 1e12
+
+
+def sampled_parity(d, C_bits, outputs: int = 20000, seed: int = 3):
+    """Part of the CPU-baseline leg: random valid outputs of one call against
+    the oracle (fp64, sampled), and every row m >= masked_m[g] compared with
+    the 0x7FC0 prefill."""
+    from oracle import oracle
+    cfg = d["cfg"]
+    mm = d["masked_m"]
+    untouched = all(bool(np.all(C_bits[g, mm[g]:] == W.SENTINEL_BF16)) for g in range(cfg.G))
+    rng = np.random.default_rng(seed)
+    valid_g = np.flatnonzero(mm > 0)
+    g = rng.choice(valid_g, outputs)
+    m = (rng.random(outputs) * mm[g]).astype(np.int64)
+    n = rng.integers(0, cfg.N, outputs)
+    idx = np.stack([g, m, n], 1).astype(np.int64)
+    ref = oracle.gemm_sampled(d["A"], d["A_sf"], d["B"], d["B_sf"], d["alpha"], idx,
+                              cfg.G, cfg.M_max, cfg.N, cfg.K)
+    vals = (C_bits[g, m, n].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ok = oracle.tolerance_ok(vals, ref, np.abs(ref).max())
+    return {"outputs": int(ok.size), "within_tolerance": int(ok.sum()),
+            "masked_rows_untouched": untouched,
+            "sample": f"{outputs} random valid (g, m, n), fp64 oracle; max|ref| over the sample"}
 
 
 def cpu_baseline(cfg, d, prob):

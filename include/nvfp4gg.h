@@ -36,6 +36,11 @@
  *     negative nvfp4gg_status without launching anything when they are bad.
  *   - Calls on one stream are thread-compatible; the SM cap set by
  *     nvfp4_gg_set_sm_count is process-wide.
+ *   - Per device the library looks up, on its first call there, the device
+ *     addresses of its static __device__ arrays (error word, signal
+ *     counters, split-K scratch) and keeps them for the life of the process.
+ *     A cudaDeviceReset invalidates them: do not call into the library on a
+ *     device after resetting it in the same process.
  */
 #ifndef NVFP4GG_H
 #define NVFP4GG_H
@@ -159,9 +164,10 @@ int nvfp4_grouped_gemm_nt_masked_splitk(const void* A, const void* A_sf, const v
  * With M_max > 64 the call runs unsplit.  Other arguments as in
  * nvfp4_grouped_gemm_nt_masked.
  * State: the partials need no initial value; the counters must be zero when
- * a split kernel starts.  They are zero when the module loads, each call
+ * a split kernel starts.  They are zero when the module loads, and each call
  * clears the ones it uses with an asynchronous memset on `stream` before its
- * launch, and the kernel leaves them at zero.
+ * launch; after a call that completed without a device-side timeout they
+ * are zero again.
  * The first call on a device looks up the scratch's device address
  * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit: make one
  * call on each device before capturing a stream.
@@ -263,6 +269,34 @@ int nvfp4_prepare_weights_swiglu(const void* B, const void* B_sf, int G, int N, 
 int nvfp4_grouped_gemm_nt_masked_swiglu(const void* A, const void* A_sf, const void* B,
                                         const void* B_sf, const float* alpha, const int* masked_m,
                                         void* C, int G, int M_max, int N, int K, void* stream);
+
+/*
+ * Dual GEMM: two GEMMs that share the activation operand A, with separate
+ * weights B1 (gate) and B2 (up) -- the "NVFP4 dual GEMM" problem of the page
+ * "LLM-Assisted Kernel Development in CuTe DSL, Gluon, Helion and Triton"
+ * (one A tile feeding two B operands; the page's derivation stacks the two
+ * B operands).  This one-time re-layout writes the prepared weights of the
+ * stacked operand straight from the two separate ones, so the caller never
+ * builds [B1; B2] itself:
+ *   B1, B2        device u8 [G][N1][K/2]   e2m1 codes of each operand
+ *   B1_sf, B2_sf  device u8 [G][N1][K/16]  their e4m3 scales
+ *   interleave 0: the layout of nvfp4_prepare_weights for the stacked
+ *                 weight [B1; B2] (N = 2 N1): nvfp4_grouped_gemm_nt_masked
+ *                 with N = 2 N1 then writes C[g][m][0 .. N1-1] = A B1^T and
+ *                 C[g][m][N1 .. 2N1-1] = A B2^T (each times alpha[g])
+ *   interleave 1: the layout of nvfp4_prepare_weights_swiglu for the same
+ *                 stacked weight (needs N1 % 64 == 0):
+ *                 nvfp4_grouped_gemm_nt_masked_swiglu (and _swiglu_quant)
+ *                 with N = 2 N1 then writes silu(alpha A B1^T) * (alpha A B2^T)
+ *   B_prep, B_sf_prep  outputs, sized by nvfp4_prepared_weight_bytes(G, 2 N1, K)
+ * The bytes written equal those of nvfp4_prepare_weights(_swiglu) on the
+ * stacked weight.  Limits: N1 % 16 == 0, 2 N1 within the GEMM's N limits,
+ * K % 256 == 0; the outputs must not overlap any input (NVFP4GG_ERR_SHAPE).
+ * Asynchronous on `stream`.
+ */
+int nvfp4_prepare_weights_dual(const void* B1, const void* B1_sf, const void* B2,
+                               const void* B2_sf, int G, int N1, int K, int interleave,
+                               void* B_prep, void* B_sf_prep, void* stream);
 
 /*
  * NVFP4 encoding of bf16 activations, GEMM2's A after the SwiGLU step (the
@@ -376,6 +410,17 @@ int nvfp4_gg_selftest_watchdog(long long timeout_ns, void* stream);
  * Time it with events on `stream` to get the dense NVFP4 tensor rate.
  */
 int nvfp4_gg_mma_peak_probe(int iters, int n, int ctas, void* stream);
+
+/*
+ * The same probe for CTA pairs (tcgen05 cta_group::2, the two SMs of a 2-CTA
+ * cluster sharing one MMA): `clusters` clusters (0 = one per pair of SMs),
+ * each issuing iters x 4 block-scaled NVFP4 MMAs of M = 256, N = n (16..256,
+ * multiple of 16), K = 64 from the leader CTA.  FLOPs of one launch:
+ * clusters * iters * 4 * 2*256*n*64.  The pair form is the one the pages'
+ * Blackwell grouped kernels use for large tiles ("LLM-Assisted Kernel
+ * Development in CuTe DSL, Gluon, Helion and Triton", NVFP4 grouped GEMM).
+ */
+int nvfp4_gg_mma_peak_probe_pair(int iters, int n, int clusters, void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* nvfp4_gg_status_string(int status);

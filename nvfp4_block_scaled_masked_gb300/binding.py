@@ -37,6 +37,7 @@ EXPORTS = (
     "nvfp4_gemv_w4a16",
     "nvfp4_grouped_gemm_nt_masked_signals",
     "nvfp4_prepare_weights_swiglu",
+    "nvfp4_prepare_weights_dual",
     "nvfp4_grouped_gemm_nt_masked_swiglu",
     "nvfp4_grouped_gemm_nt_masked_swiglu_quant",
     "nvfp4_quantize_bf16",
@@ -47,6 +48,7 @@ EXPORTS = (
     "nvfp4_gg_check_error",
     "nvfp4_gg_selftest_watchdog",
     "nvfp4_gg_mma_peak_probe",
+    "nvfp4_gg_mma_peak_probe_pair",
     "nvfp4_gg_status_string",
 )
 
@@ -92,6 +94,8 @@ def load():
     lib.nvfp4_grouped_gemm_nt_masked_signals.restype = i
     lib.nvfp4_prepare_weights_swiglu.argtypes = [vp, vp, i, i, i, vp, vp, vp]
     lib.nvfp4_prepare_weights_swiglu.restype = i
+    lib.nvfp4_prepare_weights_dual.argtypes = [vp] * 4 + [i] * 4 + [vp, vp, vp]
+    lib.nvfp4_prepare_weights_dual.restype = i
     lib.nvfp4_grouped_gemm_nt_masked_swiglu.argtypes = [vp] * 7 + [i] * 4 + [vp]
     lib.nvfp4_grouped_gemm_nt_masked_swiglu.restype = i
     lib.nvfp4_grouped_gemm_nt_masked_swiglu_quant.argtypes = [vp] * 10 + [i] * 4 + [vp]
@@ -112,6 +116,8 @@ def load():
     lib.nvfp4_gg_selftest_watchdog.restype = i
     lib.nvfp4_gg_mma_peak_probe.argtypes = [i, i, i, vp]
     lib.nvfp4_gg_mma_peak_probe.restype = i
+    lib.nvfp4_gg_mma_peak_probe_pair.argtypes = [i, i, i, vp]
+    lib.nvfp4_gg_mma_peak_probe_pair.restype = i
     lib.nvfp4_gg_status_string.argtypes = [i]
     lib.nvfp4_gg_status_string.restype = ctypes.c_char_p
     _lib = lib
@@ -207,6 +213,13 @@ def nvfp4_prepare_weights_swiglu(B, B_sf, G, N, K, B_prep, B_sf_prep, stream=Non
            "nvfp4_prepare_weights_swiglu")
 
 
+def nvfp4_prepare_weights_dual(B1, B1_sf, B2, B2_sf, G, N1, K, interleave, B_prep, B_sf_prep,
+                               stream=None):
+    _check(load().nvfp4_prepare_weights_dual(
+        _ptr(B1), _ptr(B1_sf), _ptr(B2), _ptr(B2_sf), G, N1, K, int(interleave), _ptr(B_prep),
+        _ptr(B_sf_prep), _stream(stream)), "nvfp4_prepare_weights_dual")
+
+
 def nvfp4_grouped_gemm_nt_masked_swiglu(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K,
                                         stream=None):
     _check(load().nvfp4_grouped_gemm_nt_masked_swiglu(_ptr(A), _ptr(A_sf), _ptr(B), _ptr(B_sf),
@@ -286,6 +299,11 @@ def nvfp4_gg_check_error(stream=None) -> int:
 def nvfp4_gg_mma_peak_probe(iters: int, n: int, ctas: int = 0, stream=None):
     _check(load().nvfp4_gg_mma_peak_probe(iters, n, ctas, _stream(stream)),
            "nvfp4_gg_mma_peak_probe")
+
+
+def nvfp4_gg_mma_peak_probe_pair(iters: int, n: int, clusters: int = 0, stream=None):
+    _check(load().nvfp4_gg_mma_peak_probe_pair(iters, n, clusters, _stream(stream)),
+           "nvfp4_gg_mma_peak_probe_pair")
 
 
 def nvfp4_gg_selftest_watchdog(timeout_ns: int, stream=None):

@@ -798,9 +798,24 @@ __global__ void __launch_bounds__(128, 1) mma_peak_kernel(int iters, int n, int*
     }
 }
 
-// Weight-scale re-layout: B_sf u8 [G][N][K/16] -> atoms [G][NT][K/64][32][4][4]
-// where atom byte (i, j, b) is the scale of row 128*nt + 32*j + i, K block
-// 4*kc + b (zero for rows >= N).  One thread per 16-byte atom row.
+// Where the rows of the logical weight [G][N][*] live: row r of expert g is
+// row r of src0 for r < split, else row r - split of src1, each source
+// holding `stride` rows per expert.  One weight: src0 = src1, split = stride
+// = N.  The dual GEMM's two operands (gate B1 and up B2 of N/2 rows each):
+// src0 = B1, src1 = B2, split = stride = N/2.
+struct WeightSource {
+    const uint8_t* src0;
+    const uint8_t* src1;
+    int split;
+    int stride;
+};
+
+__device__ __forceinline__ const uint8_t* weight_row(const WeightSource& w, int g, int r,
+                                                     size_t row_bytes) {
+    return r < w.split ? w.src0 + ((size_t)g * w.stride + r) * row_bytes
+                       : w.src1 + ((size_t)g * w.stride + (r - w.split)) * row_bytes;
+}
+
 // Source row of prepared weight row n: the identity, or with `swiglu` the
 // gate/up interleave the fused SwiGLU epilogue reads (N % 128 == 0): in
 // 128-row block b, lane quarter q, row l of 32 holds gate row
@@ -812,9 +827,11 @@ __device__ __forceinline__ int prepared_source_row(int n, int N, int swiglu) {
     return l < 16 ? col : (N >> 1) + col;
 }
 
-__global__ void relayout_weight_scales_kernel(const uint8_t* __restrict__ bsf,
-                                              uint8_t* __restrict__ out, int G, int N, int K,
-                                              int swiglu) {
+// Weight-scale re-layout: B_sf u8 [G][N][K/16] -> atoms [G][NT][K/64][32][4][4]
+// where atom byte (i, j, b) is the scale of row 128*nt + 32*j + i, K block
+// 4*kc + b (zero for rows >= N).  One thread per 16-byte atom row.
+__global__ void relayout_weight_scales_kernel(const WeightSource bsf, uint8_t* __restrict__ out,
+                                              int G, int N, int K, int swiglu) {
     const int NT = (N + 127) / 128;
     const int KC = K / 64;
     const long long rows = (long long)G * NT * KC * 32;
@@ -832,7 +849,7 @@ __global__ void relayout_weight_scales_kernel(const uint8_t* __restrict__ bsf,
         for (int j = 0; j < 4; ++j) {
             const int n = nt * 128 + 32 * j + i;
             wv[j] = n < N ? *reinterpret_cast<const uint32_t*>(
-                                bsf + ((size_t)g * N + prepared_source_row(n, N, swiglu)) * ks16 + 4 * kc)
+                                weight_row(bsf, g, prepared_source_row(n, N, swiglu), ks16) + 4 * kc)
                           : 0u;
         }
         *reinterpret_cast<uint4*>(out + idx * 16) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
@@ -844,9 +861,8 @@ __global__ void relayout_weight_scales_kernel(const uint8_t* __restrict__ bsf,
 // the way a 128-byte-swizzled TMA load would leave them in shared memory
 // (16-byte chunk c of row r at chunk c ^ (r % 8)), zero for rows >= N.  One
 // thread per 16-byte chunk.
-__global__ void relayout_weight_codes_kernel(const uint8_t* __restrict__ b,
-                                             uint8_t* __restrict__ out, int G, int N, int K,
-                                             int swiglu) {
+__global__ void relayout_weight_codes_kernel(const WeightSource b, uint8_t* __restrict__ out,
+                                             int G, int N, int K, int swiglu) {
     const int NT = (N + 127) / 128;
     const int KS = K / 256;
     const long long chunks = (long long)G * NT * KS * 1024;
@@ -863,7 +879,7 @@ __global__ void relayout_weight_codes_kernel(const uint8_t* __restrict__ b,
         const int n = nt * 128 + r;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (n < N)
-            v = *reinterpret_cast<const uint4*>(b + ((size_t)g * N + prepared_source_row(n, N, swiglu)) * row_bytes +
+            v = *reinterpret_cast<const uint4*>(weight_row(b, g, prepared_source_row(n, N, swiglu), row_bytes) +
                                                 (size_t)ks * 128 + c * 16);
         *reinterpret_cast<uint4*>(out + (idx >> 3) * 128 + ((c ^ (r & 7)) * 16)) = v;
     }

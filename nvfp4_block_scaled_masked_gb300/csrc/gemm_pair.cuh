@@ -446,4 +446,78 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
     }
 }
 
+// Tensor-pipe throughput probe for CTA pairs: each 2-CTA cluster issues
+// `iters` x 4 pair MMAs (M = 256: 128 rows per CTA, N = n, K = 64) from the
+// leader's thread 0 on resident shared-memory operands (zero codes, unit
+// scales written into each CTA's TMEM with tcgen05.st), then both CTAs wait
+// for the multicast commit with a bounded wait.  FLOPs per cluster:
+// iters * 4 * 2 * 256 * n * 64.
+__global__ void __launch_bounds__(128, 1) mma_peak_pair_kernel(int iters, int n, int* err,
+                                                               unsigned long long timeout_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sbase = smem_raw + (base - raw);
+    // [0, 16K) this CTA's 128 A rows, [16K, 32K) its (at most 128) B rows,
+    // then the barrier and the TMEM slot
+    constexpr int OFF_BAR = 32768, OFF_SLOT = 32776;
+    const int warp = threadIdx.x >> 5;
+    const bool leader = cluster_ctarank() == 0;
+    for (int i = threadIdx.x; i < OFF_BAR / 16; i += blockDim.x)
+        reinterpret_cast<uint4*>(sbase)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) {
+        mbar_init(base + OFF_BAR, 1);
+        fence_mbar_init();
+    }
+    fence_proxy_async_smem();
+    if (warp == 0) {
+        tmem_alloc_pair(base + OFF_SLOT, 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sbase + OFF_SLOT);
+    // scale factors: columns 256..271 (A: 4 K chunks x 4) and 272..303
+    // (B: 4 K chunks x 8), e4m3 1.0 in every byte, in this warp's lane quarter
+    {
+        uint32_t ones[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ones[i] = 0x38383838u;
+        const uint32_t q = tmem + ((uint32_t)(warp * 32) << 16);
+        tmem_st_32x32b_x16(q + 256, ones);
+        tmem_st_32x32b_x16(q + 272, ones);
+        tmem_st_32x32b_x16(q + 288, ones);
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();   // both CTAs' operands, scales and barriers are ready
+    tc_fence_after();
+    if (leader && threadIdx.x == 0) {
+        const uint32_t sfa = tmem + 256, sfb = tmem + 272;
+        const uint32_t idesc = idesc_mxf4nvf4_pair((uint32_t)n);
+        const uint64_t ad = sdesc_k_sw128(base);
+        const uint64_t bd = sdesc_k_sw128(base + 16384);
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                umma_pair_mxf4nvf4(tmem, ad + 2 * q, bd + 2 * q, idesc, sfa + 4 * q, sfb + 8 * q,
+                                   (it | q) != 0);
+        }
+        umma_commit_pair_multicast(base + OFF_BAR, 0x3);
+    }
+    if (threadIdx.x == 0) {
+        volatile int no_abort = 0;
+        wait_bounded(base + OFF_BAR, 0, &no_abort, err, timeout_ns);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
+    }
+}
+
 }  // namespace nvfp4gg

@@ -188,8 +188,7 @@ int launch_pair_variant(DeviceState* d, int slot, const GemmParams& p, cudaStrea
     }
     int ctas = d->sms;
     if (g_sm_cap > 0 && g_sm_cap < ctas) ctas = g_sm_cap;
-    ctas &= ~1;
-    if (ctas < 2) ctas = 2;
+    ctas &= ~1;   // whole pairs, never more CTAs than the cap allows
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas, 1, 1);
     cfg.blockDim = dim3(kPairThreads, 1, 1);
@@ -254,16 +253,34 @@ int nvfp4_prepared_weight_bytes(int G, int N, int K, size_t* b_bytes, size_t* sf
 
 namespace {
 
-// Weight re-layout; `swiglu` interleaves gate and up rows (N % 128 == 0).
-int prepare_weights(const void* B, const void* B_sf, int G, int N, int K, void* B_prep,
-                    void* B_sf_prep, void* stream, int swiglu) {
-    if (!B || !B_sf || !B_prep || !B_sf_prep) return NVFP4GG_ERR_NULL;
+// Weight re-layout of the logical weight [G][N][K] held by `codes` /
+// `scales`; `swiglu` interleaves gate and up rows (N % 128 == 0).  `ranges`
+// are the source buffers' byte ranges, checked against the outputs' (no
+// overlap).
+struct ByteRange {
+    const void* p;
+    size_t n;
+};
+
+bool overlaps(ByteRange a, ByteRange b) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+int prepare_weights(const WeightSource& codes, const WeightSource& scales, int G, int N, int K,
+                    void* B_prep, void* B_sf_prep, void* stream, int swiglu,
+                    const ByteRange* ranges, int nranges) {
+    if (!codes.src0 || !codes.src1 || !scales.src0 || !scales.src1 || !B_prep || !B_sf_prep)
+        return NVFP4GG_ERR_NULL;
     size_t bb = 0, sb = 0;
     int rc = nvfp4_prepared_weight_bytes(G, N, K, &bb, &sb);
     if (rc != NVFP4GG_OK) return rc;
-    if (!aligned(B, 16) || !aligned(B_sf, 16) || !aligned(B_prep, 16) || !aligned(B_sf_prep, 16))
+    if (!aligned(codes.src0, 16) || !aligned(codes.src1, 16) || !aligned(scales.src0, 16) ||
+        !aligned(scales.src1, 16) || !aligned(B_prep, 16) || !aligned(B_sf_prep, 16))
         return NVFP4GG_ERR_ALIGN;
-    if (B == B_prep || B_sf == B_sf_prep) return NVFP4GG_ERR_SHAPE;
+    const ByteRange outs[2] = {{B_prep, bb}, {B_sf_prep, sb}};
+    for (int i = 0; i < nranges; ++i)
+        if (overlaps(ranges[i], outs[0]) || overlaps(ranges[i], outs[1])) return NVFP4GG_ERR_SHAPE;
     DeviceState* d = nullptr;
     if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -271,12 +288,22 @@ int prepare_weights(const void* B, const void* B_sf, int G, int N, int K, void* 
     const long long cap = 16LL * d->sms;
     long long blocks = ((long long)(bb / 16) + threads - 1) / threads;
     relayout_weight_codes_kernel<<<(int)(blocks < cap ? blocks : cap), threads, 0, st>>>(
-        static_cast<const uint8_t*>(B), static_cast<uint8_t*>(B_prep), G, N, K, swiglu);
+        codes, static_cast<uint8_t*>(B_prep), G, N, K, swiglu);
     if (cudaGetLastError() != cudaSuccess) return NVFP4GG_ERR_CUDA;
     blocks = ((long long)(sb / 16) + threads - 1) / threads;
     relayout_weight_scales_kernel<<<(int)(blocks < cap ? blocks : cap), threads, 0, st>>>(
-        static_cast<const uint8_t*>(B_sf), static_cast<uint8_t*>(B_sf_prep), G, N, K, swiglu);
+        scales, static_cast<uint8_t*>(B_sf_prep), G, N, K, swiglu);
     return cuda_status(cudaGetLastError());
+}
+
+int prepare_single(const void* B, const void* B_sf, int G, int N, int K, void* B_prep,
+                   void* B_sf_prep, void* stream, int swiglu) {
+    if (!B || !B_sf || !B_prep || !B_sf_prep) return NVFP4GG_ERR_NULL;
+    const uint8_t* b = static_cast<const uint8_t*>(B);
+    const uint8_t* s = static_cast<const uint8_t*>(B_sf);
+    const WeightSource codes{b, b, N, N}, scales{s, s, N, N};
+    const ByteRange in[2] = {{B, (size_t)G * N * (K / 2)}, {B_sf, (size_t)G * N * (K / 16)}};
+    return prepare_weights(codes, scales, G, N, K, B_prep, B_sf_prep, stream, swiglu, in, 2);
 }
 
 }  // namespace
@@ -285,13 +312,33 @@ extern "C" {
 
 int nvfp4_prepare_weights(const void* B, const void* B_sf, int G, int N, int K, void* B_prep,
                           void* B_sf_prep, void* stream) {
-    return prepare_weights(B, B_sf, G, N, K, B_prep, B_sf_prep, stream, 0);
+    return prepare_single(B, B_sf, G, N, K, B_prep, B_sf_prep, stream, 0);
 }
 
 int nvfp4_prepare_weights_swiglu(const void* B, const void* B_sf, int G, int N, int K,
                                  void* B_prep, void* B_sf_prep, void* stream) {
     if (N % 128 != 0) return NVFP4GG_ERR_SHAPE;
-    return prepare_weights(B, B_sf, G, N, K, B_prep, B_sf_prep, stream, 1);
+    return prepare_single(B, B_sf, G, N, K, B_prep, B_sf_prep, stream, 1);
+}
+
+int nvfp4_prepare_weights_dual(const void* B1, const void* B1_sf, const void* B2, const void* B2_sf,
+                               int G, int N1, int K, int interleave, void* B_prep, void* B_sf_prep,
+                               void* stream) {
+    if (!B1 || !B1_sf || !B2 || !B2_sf || !B_prep || !B_sf_prep) return NVFP4GG_ERR_NULL;
+    if (interleave != 0 && interleave != 1) return NVFP4GG_ERR_SHAPE;
+    if (N1 < 1 || N1 > (1 << 19)) return NVFP4GG_ERR_SHAPE;
+    const int N = 2 * N1;
+    if (check_gemm_shape(G, 1, N, K) != NVFP4GG_OK || N1 % NVFP4GG_N_ALIGN != 0 ||
+        (interleave && N % 128 != 0))
+        return NVFP4GG_ERR_SHAPE;
+    const uint8_t* b1 = static_cast<const uint8_t*>(B1);
+    const uint8_t* b2 = static_cast<const uint8_t*>(B2);
+    const uint8_t* s1 = static_cast<const uint8_t*>(B1_sf);
+    const uint8_t* s2 = static_cast<const uint8_t*>(B2_sf);
+    const WeightSource codes{b1, b2, N1, N1}, scales{s1, s2, N1, N1};
+    const size_t cb = (size_t)G * N1 * (K / 2), sb = (size_t)G * N1 * (K / 16);
+    const ByteRange in[4] = {{B1, cb}, {B2, cb}, {B1_sf, sb}, {B2_sf, sb}};
+    return prepare_weights(codes, scales, G, N, K, B_prep, B_sf_prep, stream, interleave, in, 4);
 }
 
 }  // extern "C"
@@ -401,7 +448,10 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
         return narrow ? launch_variant<kNarrowTT, kNarrowStages, true>(d, 3, p, st)
                       : launch_variant<kWideTT, kWideStages, true>(d, 4, p, st);
     if (narrow) return launch_variant<kNarrowTT, kNarrowStages>(d, 0, p, st);
-    if (pair) return launch_pair_variant<kPairTT, kPairStages>(d, 2, p, st);
+    // a cap of one SM leaves no room for a CTA pair: the single-CTA kernel
+    // (same token tile bound, same tensor maps) runs the call instead
+    const bool pair_fits = g_sm_cap == 0 || g_sm_cap >= 2;
+    if (pair && pair_fits) return launch_pair_variant<kPairTT, kPairStages>(d, 2, p, st);
     return launch_variant<kWideTT, kWideStages>(d, 1, p, st);
 }
 
@@ -716,6 +766,36 @@ int nvfp4_gg_mma_peak_probe(int iters, int n, int ctas, void* stream) {
     return cuda_status(cudaGetLastError());
 }
 
+int nvfp4_gg_mma_peak_probe_pair(int iters, int n, int clusters, void* stream) {
+    if (iters < 1 || iters > (1 << 24) || n < 16 || n > 256 || n % 16 != 0 || clusters < 0)
+        return NVFP4GG_ERR_SHAPE;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != NVFP4GG_OK) return rc;
+    // operands use 33 KB; asking for more than half an SM's shared memory
+    // keeps every CTA of the probe on an SM of its own (no CTA waits in
+    // tcgen05.alloc for a CTA of another cluster)
+    constexpr int kSmem = 120 * 1024;
+    if (cudaFuncSetAttribute(mma_peak_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmem) != cudaSuccess)
+        return NVFP4GG_ERR_CUDA;
+    const int max_clusters = d->sms / 2;
+    const int ncl = (clusters == 0 || clusters > max_clusters) ? max_clusters : clusters;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * ncl, 1, 1);
+    cfg.blockDim = dim3(128, 1, 1);
+    cfg.dynamicSmemBytes = kSmem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, mma_peak_pair_kernel, iters, n, d->err, g_timeout_ns));
+}
+
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
@@ -776,6 +856,9 @@ extern "C" int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(
         DeviceState* d = nullptr;
         if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
         split = auto_split(d, tiles, K);
+        // auto_split keeps tiles x split <= SMs, below the slot count on
+        // every GPU with at most NVFP4GG_NOALLOC_MAX_SLOTS SMs (GB300: 152),
+        // so this guard only acts on larger GPUs
         if (tiles * split > slots) split = (int)(slots / tiles);
     }
     if (split <= 1)

@@ -168,6 +168,37 @@ def draw_scales(rng: np.random.Generator, shape) -> np.ndarray:
     return SCALE_BYTES[_uniform_index(rng, n, len(SCALE_BYTES))].reshape(shape)
 
 
+# Scale-byte sets for the full-range inputs: every finite non-negative e4m3
+# byte (0x00 zero, 0x01..0x07 subnormal, up to 0x7E = 448; 0x7F is NaN), the
+# subnormals with zero, and the top binades.
+SCALE_SETS = {
+    "all": np.arange(0x00, 0x7F, dtype=np.uint8),
+    "subnormal": np.arange(0x00, 0x08, dtype=np.uint8),
+    "large": np.arange(0x70, 0x7F, dtype=np.uint8),
+    "powers": SCALE_BYTES,
+}
+
+
+def generate_full_range(cfg: Config, seed: int, a_scales: str = "all",
+                        b_scales: str = "all") -> dict:
+    """Inputs over the whole NVFP4 domain, in the layouts of generate(): both
+    nibbles of every code byte uniform over all 16 e2m1 codes (negative zero
+    0x8 included), scale bytes uniform over SCALE_SETS[a_scales] for A_sf and
+    SCALE_SETS[b_scales] for B_sf, alpha uniform in [0.5, 2).  masked_m as the
+    config says; C prefilled with 0x7FC0."""
+    G, M, N, K = cfg.G, cfg.M_max, cfg.N, cfg.K
+    rng = np.random.default_rng(seed)
+    masked_m = draw_masked_m(cfg, rng)
+    alpha = rng.uniform(0.5, 2.0, size=G).astype(np.float32)
+    sa, sb = SCALE_SETS[a_scales], SCALE_SETS[b_scales]
+    A = rng.integers(0, 256, size=(G, M, K // 2), dtype=np.uint8)
+    A_sf = sa[_uniform_index(rng, G * M * (K // 16), len(sa))].reshape(G, M, K // 16)
+    B = rng.integers(0, 256, size=(G, N, K // 2), dtype=np.uint8)
+    B_sf = sb[_uniform_index(rng, G * N * (K // 16), len(sb))].reshape(G, N, K // 16)
+    return dict(cfg=cfg, masked_m=masked_m, alpha=alpha, A=A, A_sf=A_sf, B=B, B_sf=B_sf,
+                C_init=np.full((G, M, N), SENTINEL_BF16, dtype=np.uint16))
+
+
 def generate(cfg: Config, seed: int | None = None, poison: bool = False,
              with_b: bool = True) -> dict:
     """All inputs of one call, as NumPy arrays in the plain layouts:

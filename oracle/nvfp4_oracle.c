@@ -87,11 +87,23 @@ uint16_t nvfp4o_bf16_rne(double x) {
     return (uint16_t)(u >> 16);
 }
 
+/* The 16 e2m1 values as a lookup table, indexed by the 4-bit code: codes
+ * 0..7 are +0, 0.5, 1, 1.5, 2, 3, 4, 6 (OCP FP4 E2M1), codes 8..15 the same
+ * magnitudes negated (8 is -0).  Elements are decoded through this table;
+ * the bit-field function above is the independent statement it is pinned
+ * against. */
+static const double kE2M1[16] = {
+    0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0,
+    -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0,
+};
+
+double nvfp4o_e2m1_table(int code) { return kE2M1[code & 15]; }
+
 /* Value of element k of the packed row `row` (K/2 bytes). */
 static double elem(const uint8_t* row, const uint8_t* sf_row, int k) {
     int byte = row[k >> 1];
     int code = (k & 1) ? (byte >> 4) : (byte & 15);
-    return nvfp4o_e2m1_value(code) * nvfp4o_e4m3_value(sf_row[k >> 4]);
+    return kE2M1[code] * nvfp4o_e4m3_value(sf_row[k >> 4]);
 }
 
 int nvfp4o_max_threads(void) {

@@ -65,6 +65,8 @@ def _load():
         u8p = ctypes.POINTER(ctypes.c_uint8)
         lib.nvfp4o_e2m1_value.restype = ctypes.c_double
         lib.nvfp4o_e2m1_value.argtypes = [ctypes.c_int]
+        lib.nvfp4o_e2m1_table.restype = ctypes.c_double
+        lib.nvfp4o_e2m1_table.argtypes = [ctypes.c_int]
         lib.nvfp4o_e4m3_value.restype = ctypes.c_double
         lib.nvfp4o_e4m3_value.argtypes = [ctypes.c_int]
         lib.nvfp4o_bf16_rne.restype = ctypes.c_uint16
@@ -88,7 +90,14 @@ def _u8(a):
 
 
 def e2m1_value(code: int) -> float:
+    """e2m1 value from the code's bit fields (sign, exponent, mantissa)."""
     return _load().nvfp4o_e2m1_value(int(code))
+
+
+def e2m1_table_value(code: int) -> float:
+    """Entry `code` of the C oracle's 16-entry e2m1 table, through which it
+    decodes every element."""
+    return _load().nvfp4o_e2m1_table(int(code))
 
 
 def e4m3_value(byte: int) -> float:

@@ -245,3 +245,24 @@ def test_gemv_argument_checks(lib):
     assert f(*a) == binding.ERR_ALIGN
     a = list(args); a[4] = None
     assert f(*a) == binding.ERR_NULL
+
+
+def test_prepare_weights_dual_argument_checks(lib):
+    f = lib.nvfp4_prepare_weights_dual
+    # B1, B1_sf, B2, B2_sf, G, N1, K, interleave, B_prep, B_sf_prep, stream
+    big = 1 << 24
+    args = [FAKE, FAKE + big, FAKE + 2 * big, FAKE + 3 * big, 2, 128, 512, 1,
+            FAKE + 4 * big, FAKE + 5 * big, None]
+    for k in (0, 1, 2, 3, 8, 9):
+        a = list(args); a[k] = None
+        assert f(*a) == binding.ERR_NULL
+    a = list(args); a[5] = 72                     # N1 % 16 != 0
+    assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[5] = 96                     # interleaved needs 2 N1 % 128 == 0
+    assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[7] = 2                      # interleave is 0 or 1
+    assert f(*a) == binding.ERR_SHAPE
+    a = list(args); a[2] = FAKE + 2 * big + 8     # misaligned B2
+    assert f(*a) == binding.ERR_ALIGN
+    a = list(args); a[8] = FAKE + 2 * big + 4096  # output overlaps B2
+    assert f(*a) == binding.ERR_SHAPE

@@ -243,19 +243,31 @@ def test_host_buffer_entry_point_matches_device_path(lib, pinned_in, pinned_out)
     check_full(d, hC.numpy().view(np.uint16))
 
 
-def test_sm_count_cap_gives_identical_results(lib):
+@pytest.mark.parametrize("G,M_max,N,K,masked", [
+    (3, 200, 384, 512, [200, 5, 130]),      # single-CTA wide kernel (N % 256 != 0)
+    (3, 200, 512, 768, [200, 5, 130]),      # CTA-pair kernel (automatic mode)
+])
+def test_sm_count_cap_gives_identical_results(lib, G, M_max, N, K, masked):
+    """The sm_count cap bounds the CTAs of a launch.  Caps of 7 and 152 run
+    the same kernel family (pairs: 6 CTAs), so the bits equal the uncapped
+    call's; a cap of 1 leaves no room for a pair and runs the single-CTA
+    kernel, equal within the tolerance."""
     from nvfp4_block_scaled_masked_gb300.device import Problem
-    d = W.generate(W.custom(3, 200, 384, 512, masked_m=[200, 5, 130]), seed=8)
+    d = W.generate(W.custom(G, M_max, N, K, masked_m=masked), seed=8 + N)
     prob = Problem(d)
     prob.run()
     ref = prob.C_bits()
+    pair_shape = N % 256 == 0
     try:
         for cap in (1, 7):
             lib.nvfp4_gg_set_sm_count(cap)
             prob.reset_C()
             prob.run()
             assert lib.nvfp4_gg_check_error() == 0
-            np.testing.assert_array_equal(prob.C_bits(), ref)
+            if cap == 1 and pair_shape:
+                check_full(d, prob.C_bits())
+            else:
+                np.testing.assert_array_equal(prob.C_bits(), ref)
     finally:
         lib.nvfp4_gg_set_sm_count(0)
     check_full(d, ref)
@@ -264,6 +276,8 @@ def test_sm_count_cap_gives_identical_results(lib):
 def test_mma_peak_probe_runs_clean(lib):
     lib.nvfp4_gg_mma_peak_probe(64, 256)
     lib.nvfp4_gg_mma_peak_probe(64, 16, 3)
+    lib.nvfp4_gg_mma_peak_probe_pair(64, 256)
+    lib.nvfp4_gg_mma_peak_probe_pair(64, 32, 3)
     assert lib.nvfp4_gg_check_error() == 0
 
 

@@ -39,6 +39,18 @@ def test_e2m1_all_codes_match_ocp_table():
     np.testing.assert_array_equal(oracle.E2M1_TABLE, [oracle.e2m1_value(c) for c in range(16)])
 
 
+def test_e2m1_decode_table_matches_ocp_and_bit_fields():
+    """The C oracle decodes elements through a 16-entry table; every entry
+    equals the OCP magnitude with the code's sign and the bit-field closed
+    form, signed zero included."""
+    mags = [Fraction(x) for x in OCP["e2m1_magnitudes_by_low3bits"]]
+    for code in range(16):
+        t = oracle.e2m1_table_value(code)
+        assert t == float(mags[code & 7] * (-1 if code & 8 else 1)), code
+        assert np.copysign(1.0, t) == (-1.0 if code & 8 else 1.0), code
+        assert t == oracle.e2m1_value(code)
+
+
 def test_e4m3_all_bytes_match_torch_float8_e4m3fn():
     lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
     got = np.array([oracle.e4m3_value(b) for b in range(256)])
