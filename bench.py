@@ -59,7 +59,7 @@ def load_peaks():
 # Sources each kernel family is compiled from: a change to any of them makes
 # that family's recorded traffic stale.
 KERNEL_SOURCES = {
-    "gemm": ("ptx.cuh", "quant.cuh", "gemm.cuh", "gemm_pair.cuh", "nvfp4gg.cu"),
+    "gemm": ("ptx.cuh", "quant.cuh", "gemm.cuh", "gemm_pair.cuh", "gemm_tok_pair.cuh", "nvfp4gg.cu"),
     "gemv": ("gemv.cuh", "nvfp4gg.cu"),
 }
 
@@ -337,9 +337,9 @@ def main():
     ap.add_argument("--swiglu-quant", action="store_true",
                     help="time the fused GEMM1 + SwiGLU entry point that also writes GEMM2's "
                          "NVFP4 activations (codes + scales of the N/2 columns)")
-    ap.add_argument("--pair-mode", default="auto", choices=["auto", "on", "off"],
-                    help="prefill kernel family: CTA pairs (on), single CTAs (off), or the "
-                         "library's automatic choice")
+    ap.add_argument("--pair-mode", default="auto", choices=["auto", "on", "off", "token"],
+                    help="prefill kernel family: CTA pairs (on), single CTAs (off), token-major "
+                         "CTA pairs (token), or the library's automatic choice")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -386,7 +386,7 @@ def main():
     stream = torch.cuda.current_stream()
 
     # one-time weight re-layout, timed separately (median of 5)
-    binding.nvfp4_gg_set_pair_mode({"off": 0, "on": 1, "auto": 2}[args.pair_mode])
+    binding.nvfp4_gg_set_pair_mode({"off": 0, "on": 1, "auto": 2, "token": 3}[args.pair_mode])
     prob = Problem(d, keep_raw_weights=True)
     prep_ms = []
     for _ in range(5):

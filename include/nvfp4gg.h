@@ -373,16 +373,22 @@ int nvfp4_gg_set_sm_count(int sm_count);
 
 /*
  * Kernel family for experts with M_max > 64 (prefill sizes).
- *   mode 0: one CTA per 128 weight rows.
+ *   mode 0: one CTA per 128 weight rows (token tiles of up to 192).
  *   mode 1: when N is a multiple of 256, the two CTAs of a 2-CTA cluster
  *           share one MMA of 256 weight rows (each CTA stages 128 weight
  *           rows and half of the token rows).
- *   mode 2 (default): CTA pairs when N % 256 == 0 and M_max <= 256, else
- *           one CTA per 128 weight rows.  Measured on GB300: pairs are
- *           ~8 % faster on bandwidth-bound prefill shapes (few token tiles
- *           per expert) and ~2 % slower on compute-heavy ones.
+ *   mode 2 (default): automatic.  N % 256 == 0 and M_max <= 256: mode 1;
+ *           N % 256 == 0 and M_max > 256: mode 3; else mode 0.  Measured on
+ *           GB300: pairs are ~8 % faster on bandwidth-bound prefill shapes
+ *           (few token tiles per expert); compute-heavy experts run fastest
+ *           on the token-major pairs.
+ *   mode 3: when N is a multiple of 256 and M_max >= 128, token-major CTA
+ *           pairs: one MMA of 256 tokens (128 per CTA) by 256 weight rows,
+ *           for experts with many valid rows.
+ * Calls with per-expert signals, the SwiGLU epilogue or the packed-rows
+ * layout, and calls capped to one SM, run on the single-CTA kernels.
  * Results are equal up to fp32 summation order.  Process-wide.
- * NVFP4GG_ERR_SHAPE unless 0, 1 or 2.
+ * NVFP4GG_ERR_SHAPE unless 0, 1, 2 or 3.
  */
 int nvfp4_gg_set_pair_mode(int mode);
 

@@ -281,7 +281,7 @@ def nvfp4_gg_set_sm_count(sm_count: int):
     _check(load().nvfp4_gg_set_sm_count(sm_count), "nvfp4_gg_set_sm_count")
 
 
-PAIR_OFF, PAIR_ON, PAIR_AUTO = 0, 1, 2
+PAIR_OFF, PAIR_ON, PAIR_AUTO, PAIR_TOKEN_MAJOR = 0, 1, 2, 3
 
 
 def nvfp4_gg_set_pair_mode(mode):

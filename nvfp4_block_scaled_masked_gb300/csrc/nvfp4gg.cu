@@ -10,6 +10,7 @@
 
 #include "gemm.cuh"
 #include "gemm_pair.cuh"
+#include "gemm_tok_pair.cuh"
 #include "gemv.cuh"
 #include "nvfp4gg.h"
 
@@ -35,7 +36,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 int g_sm_cap = 0;
-int g_pair_mode = 2;   // CTA-pair prefill kernel: 0 off, 1 on, 2 automatic (see nvfp4gg.h)
+int g_pair_mode = 2;   // prefill kernel family: 0 single, 1 pairs, 2 automatic, 3 token-major pairs (nvfp4gg.h)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 unsigned long long g_timeout_ns = 2000000000ull;   // 2 s per device-side wait
 
@@ -204,6 +205,75 @@ int launch_pair_variant(DeviceState* d, int slot, const GemmParams& p, cudaStrea
     return cuda_status(cudaLaunchKernelEx(&cfg, kern, p));
 }
 
+// Tensor map of the prepared weight tiles as a 2-D u8 array of 128-byte rows
+// (16 KB tiles = 128 rows; the bytes are already swizzled, so the map does not
+// swizzle), for the token-major pair kernel's tiled loads.  Cached per buffer.
+struct WeightMap {
+    const void* B = nullptr;
+    uint64_t rows = 0;
+    int dev = -1;
+    CUtensorMap m;
+};
+constexpr int kWeightMapCache = 4;
+WeightMap g_wmaps[kWeightMapCache];
+int g_wmaps_next = 0;
+
+int weight_map(const void* B, uint64_t rows, CUtensorMap* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4GG_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int i = 0; i < kWeightMapCache; ++i) {
+        if (g_wmaps[i].B == B && g_wmaps[i].rows == rows && g_wmaps[i].dev == dev) {
+            *out = g_wmaps[i].m;
+            return NVFP4GG_OK;
+        }
+    }
+    WeightMap& w = g_wmaps[g_wmaps_next];
+    g_wmaps_next = (g_wmaps_next + 1) % kWeightMapCache;
+    w.B = nullptr;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(&w.m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(B), dims, strides,
+                          box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return NVFP4GG_ERR_CUDA;
+    w.rows = rows;
+    w.dev = dev;
+    w.B = B;
+    *out = w.m;
+    return NVFP4GG_OK;
+}
+
+int launch_tok_pair(DeviceState* d, int slot, const GemmParams& p, const CUtensorMap& tm_w,
+                    cudaStream_t stream) {
+    using Cfg = TokPairCfg;
+    if (!d->attr_set[slot]) {
+        if (cudaFuncSetAttribute(gemm_nt_masked_tok_pair_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 Cfg::SMEM_BYTES) != cudaSuccess)
+            return NVFP4GG_ERR_CUDA;
+        d->attr_set[slot] = true;
+    }
+    int ctas = d->sms;
+    if (g_sm_cap > 0 && g_sm_cap < ctas) ctas = g_sm_cap;
+    ctas &= ~1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas, 1, 1);
+    cfg.blockDim = dim3(kTokThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cuda_status(cudaLaunchKernelEx(&cfg, gemm_nt_masked_tok_pair_kernel, p, tm_w));
+}
+
 // Decode-sized experts (M_max <= 64): token tiles of at most 32, a deep ring
 // for the weight stream.  Larger experts: token tiles of up to 192, so that a
 // prefill expert's rows usually fit one tile and its weights stream once, and
@@ -218,6 +288,8 @@ constexpr int kPairTT = 192, kPairStages = 6;
 // token tiles per expert: the weight stream dominates and the pair's halved
 // token staging and deeper ring pay); compute-heavy experts stay single.
 constexpr int kPairAutoMaxRows = 256;
+// Token-major pairs: 128 token rows per CTA (one tensor-map box).
+constexpr int kTokTT = 128;
 
 }  // namespace
 
@@ -398,9 +470,16 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
     if ((rc = device_state(&d)) != NVFP4GG_OK) return rc;
 
     const bool narrow = M_max <= 64;
-    const bool pair = !narrow && !swiglu && !signals && N % 256 == 0 &&
+    // a cap of one SM leaves no room for a CTA pair: the single-CTA kernel
+    // (same token tile bound, same tensor maps) runs the call instead
+    const bool pair_fits = g_sm_cap == 0 || g_sm_cap >= 2;
+    const bool pairable = !narrow && !swiglu && !signals && N % 256 == 0 && pair_fits;
+    // token-major pairs (256 x 256 MMA tiles) for compute-heavy experts
+    const bool tok = pairable && M_total == 0 && M_max >= 128 &&
+                     (g_pair_mode == 3 || (g_pair_mode == 2 && M_max > kPairAutoMaxRows));
+    const bool pair = pairable && !tok &&
                       (g_pair_mode == 1 || (g_pair_mode == 2 && M_max <= kPairAutoMaxRows));
-    const int tt_max = narrow ? kNarrowTT : pair ? kPairTT : kWideTT;
+    const int tt_max = narrow ? kNarrowTT : tok ? kTokTT : pair ? kPairTT : kWideTT;
     GemmParams p;
     std::memset(&p, 0, sizeof(p));
     // packed rows (M_total > 0): one group of M_total rows; else [G][M_max]
@@ -448,10 +527,13 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
         return narrow ? launch_variant<kNarrowTT, kNarrowStages, true>(d, 3, p, st)
                       : launch_variant<kWideTT, kWideStages, true>(d, 4, p, st);
     if (narrow) return launch_variant<kNarrowTT, kNarrowStages>(d, 0, p, st);
-    // a cap of one SM leaves no room for a CTA pair: the single-CTA kernel
-    // (same token tile bound, same tensor maps) runs the call instead
-    const bool pair_fits = g_sm_cap == 0 || g_sm_cap >= 2;
-    if (pair && pair_fits) return launch_pair_variant<kPairTT, kPairStages>(d, 2, p, st);
+    if (tok) {
+        CUtensorMap tm_w;
+        const uint64_t rows = (uint64_t)G * p.NT * p.KS * 128;
+        if ((rc = weight_map(B, rows, &tm_w)) != NVFP4GG_OK) return rc;
+        return launch_tok_pair(d, 5, p, tm_w, st);
+    }
+    if (pair) return launch_pair_variant<kPairTT, kPairStages>(d, 2, p, st);
     return launch_variant<kWideTT, kWideStages>(d, 1, p, st);
 }
 
@@ -717,7 +799,7 @@ int nvfp4_gg_set_sm_count(int sm_count) {
 }
 
 int nvfp4_gg_set_pair_mode(int mode) {
-    if (mode < 0 || mode > 2) return NVFP4GG_ERR_SHAPE;
+    if (mode < 0 || mode > 3) return NVFP4GG_ERR_SHAPE;
     std::lock_guard<std::mutex> lock(g_mu);
     g_pair_mode = mode;
     return NVFP4GG_OK;

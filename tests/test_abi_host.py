@@ -147,8 +147,9 @@ def test_noalloc_splitk_argument_checks(lib):
 def test_sm_cap_and_watchdog_argument_checks(lib):
     assert lib.nvfp4_gg_set_sm_count(-1) == binding.ERR_SHAPE
     assert lib.nvfp4_gg_set_sm_count(0) == binding.OK
-    assert lib.nvfp4_gg_set_pair_mode(3) == binding.ERR_SHAPE
+    assert lib.nvfp4_gg_set_pair_mode(4) == binding.ERR_SHAPE
     assert lib.nvfp4_gg_set_pair_mode(-1) == binding.ERR_SHAPE
+    assert lib.nvfp4_gg_set_pair_mode(3) == binding.OK   # token-major pairs
     assert lib.nvfp4_gg_set_pair_mode(1) == binding.OK
     assert lib.nvfp4_gg_set_pair_mode(0) == binding.OK
     assert lib.nvfp4_gg_set_pair_mode(2) == binding.OK   # the default: automatic

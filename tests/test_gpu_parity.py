@@ -140,6 +140,24 @@ def test_prefill_variants_pair_and_single(lib, G, M_max, N, K, masked, pair):
         lib.nvfp4_gg_set_pair_mode(lib.PAIR_AUTO)
 
 
+@pytest.mark.parametrize("G,M_max,N,K,masked", [
+    (3, 300, 512, 1536, [300, 0, 129]),      # 2 token tiles (the second CTA's rows of the
+                                             # last one wholly past M_max), 6 stages > ring
+    (2, 256, 768, 2048, [256, 200]),         # 3 weight-block pairs, 8 stages
+    (1, 128, 256, 256, [1]),                 # one stage, one valid row
+    (4, 512, 256, 7168, [512, 511, 0, 257]),  # 28 stages, ragged token tiles, empty expert
+])
+def test_token_major_pair_kernel(lib, G, M_max, N, K, masked):
+    """Token-major CTA pairs (256 tokens x 256 weight rows per MMA), forced
+    with pair mode 3 on small shapes; chosen automatically for M_max > 256."""
+    d = W.generate(W.custom(G, M_max, N, K, masked_m=masked), seed=3 * G + N + K)
+    lib.nvfp4_gg_set_pair_mode(lib.PAIR_TOKEN_MAJOR)
+    try:
+        check_full(d, run_gpu(d))
+    finally:
+        lib.nvfp4_gg_set_pair_mode(lib.PAIR_AUTO)
+
+
 @pytest.mark.parametrize("key", ["c4", "c5"])
 def test_full_size_sampled_pair_kernel(lib, key):
     lib.nvfp4_gg_set_pair_mode(True)

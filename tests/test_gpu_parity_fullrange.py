@@ -5,7 +5,8 @@ leave out the negative-zero code.  Here every e2m1 code (0x8 = -0 included)
 and every finite non-negative e4m3 scale byte 0x00..0x7E (zero, the
 subnormals 0x01..0x07, mantissa bits, up to 448) reach the tensor cores of
 each kernel family: the decode kernel (token tiles of 32), the 192-wide
-single-CTA kernel and the CTA-pair kernel, including K = 7168.  Scale
+single-CTA kernel, the CTA-pair kernel and the token-major CTA-pair kernel,
+including K = 7168.  Scale
 regimes run as separate calls (all bytes; subnormal x subnormal; subnormal x
 large; large x large), so a kernel that mis-decoded subnormal or large scales
 could not hide behind the tolerance's absolute term (1e-4 of the call's
@@ -85,6 +86,7 @@ SHAPES = [
     ("wide", 2, 200, 512, 7168, [200, 129], 0),
     ("pair", 2, 200, 512, 7168, [200, 129], 1),
     ("pair", 3, 256, 768, 1024, [256, 31, 0], 1),
+    ("token-major pair", 2, 300, 512, 7168, [300, 129], 3),
 ]
 
 
