@@ -12,16 +12,17 @@
 // tiles can.  The accumulator holds 256 fp32 columns (one buffer), so
 // five TMEM scale-factor regions fit beside it: one per ring stage.
 //
-// Roles (480 threads per CTA; a role's warp walks the stages with
+// Roles (512 threads per CTA; a role's warp walks the stages with
 // warp-uniform values and an elected lane issues the single-thread
-// instructions):
-//   warp 0        weight producer: the scale atoms of both weight blocks of
-//                 the pair (4 KB, bulk copies into this CTA) and this CTA's
-//                 16 KB weight tile (tiled TMA whose completion is counted on
-//                 the leader's `full` barrier).
-//   warp 2        token producer: this CTA's 128 token scale rows (TMA, this
-//                 CTA's `sfull`) and its 128 token rows (TMA counted on the
-//                 leader's `full`).
+// instructions).  Each producer issues one copy per stage: measured on
+// GB300, a thread's copies per stage, not their bytes, bound the ring.
+//   warp 0        weight producer: this CTA's 16 KB weight tile (tiled TMA
+//                 whose completion is counted on the leader's `full`).
+//   warp 2        token producer: this CTA's 128 token rows (same).
+//   warp 15       scale producer: its weight block's 2 KB of scale atoms,
+//                 multicast to both CTAs (each CTA's scale warps need all
+//                 256 rows' scales), and its 128 token scale rows; both
+//                 complete this CTA's `sfull`.
 //   warp 1        TMEM (allocated for the pair).  Leader: the MMA warp, 4
 //                 pair MMAs per stage after one wait on `full` (both CTAs'
 //                 operand tiles) and one on `sfready` (both CTAs' scale
@@ -47,7 +48,7 @@
 
 namespace nvfp4gg {
 
-constexpr int kTokThreads = 480;
+constexpr int kTokThreads = 512;
 
 struct TokPairCfg {
     static constexpr int STAGES = 5;
@@ -76,9 +77,12 @@ struct TokPairCfg {
     static constexpr int NUM_BARS = 4 * STAGES + 3;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_TAB = (OFF_MISC + 16 + 15) & ~15;
-    static constexpr int TAB_BYTES = (2 * kGroupsMax + 1) * 4;   // cum, gm
-    static constexpr int SMEM_BYTES = OFF_TAB + TAB_BYTES + 1024;
-    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    // cum[G + 1], gm[G]: sized per launch (plus alignment slack)
+    static constexpr int SMEM_FIXED = OFF_TAB + 4 + 1024;
+    static constexpr int SMEM_LIMIT = 232448;
+    static_assert(SMEM_FIXED + 8 <= SMEM_LIMIT, "shared memory budget");
+    static constexpr int MAX_GROUPS = (SMEM_LIMIT - SMEM_FIXED) / 8;
+    static int smem_bytes(int G) { return SMEM_FIXED + 8 * G; }
     static_assert(OFF_W % 1024 == 0 && OFF_T % 1024 == 0, "128-byte swizzle alignment");
 };
 
@@ -125,12 +129,12 @@ gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams p,
     uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     int* cum = reinterpret_cast<int*>(sbase + Cfg::OFF_TAB);
-    int* gm = cum + kGroupsMax + 1;
+    int* gm = cum + p.G + 1;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(bar_full + 8 * s, 2);
-            mbar_init(bar_sfull + 8 * s, 2);
+            mbar_init(bar_sfull + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, 1);
             mbar_init(bar_sfready + 8 * s, 8);
         }
@@ -190,9 +194,16 @@ gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams p,
     // the leader's full barriers, as addresses this CTA's TMA can signal
     const uint32_t full_leader = leader ? bar_full : mapa_shared(bar_full, 0);
 
-    if (warp == 0 || warp == 2) {
+    if (warp == 0 || warp == 2 || warp == 15) {
         // ----------------------------------------------------------- producers
-        const bool weights = warp == 0;
+        // One copy per stage per producer warp: an issuing thread with
+        // several copies per stage was measured to be the ring's bound.
+        //   warp 0:  this CTA's weight tile (leader's `full`)
+        //   warp 2:  this CTA's token tile (leader's `full`)
+        //   warp 15: this CTA's weight block's scale atoms, multicast to both
+        //            CTAs, and its token scale rows (this CTA's `sfull`, which
+        //            also receives the peer's atoms)
+        const int role = warp == 0 ? 0 : warp == 2 ? 1 : 2;
         const uint64_t pol_stream = policy_evict_first();
         int s = 0;
         uint32_t ph = 0;
@@ -200,51 +211,51 @@ gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams p,
         bool ok = true;
         for (int tile = cid; tile < total && ok; tile += ncl) {
             const TileCoord tc = decode_tok_tile(cum, gm, p.G, tile);
-            const int nt0 = 2 * tc.nt;                       // the pair's first weight block
-            const size_t wsf0 = ((size_t)tc.g * p.NT + nt0) * (size_t)(p.KS * 4);   // atom index
+            const int nt = 2 * tc.nt + (int)rank;                // this CTA's weight block
+            const size_t wsf0 = ((size_t)tc.g * p.NT + nt) * (size_t)(p.KS * 4);   // atom index
             // row of this CTA's weight tile in the prepared-tile map, stage 0
-            const int wrow = (int)((((size_t)tc.g * p.NT + nt0 + rank) * p.KS) * 128);
+            const int wrow = (int)((((size_t)tc.g * p.NT + nt) * p.KS) * 128);
             const int trow = tc.t0 + 128 * (int)rank;
             for (int ks = 0; ks < p.KS; ++ks) {
                 ok = __all_sync(0xffffffffu, wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort_flag,
                                                           p.err, p.timeout_ns));
                 if (!ok) break;
-                const uint32_t sb = bar_sfull + 8 * s;
                 const uint32_t fl = full_leader + 8 * s;
                 if (!elect_one()) {
-                } else if (weights) {
-                    mbar_arrive_expect_tx(sb, Cfg::WSF_STAGE);
-                    const uint8_t* a0 = p.wsf + (wsf0 + 4 * (size_t)ks) * 512;
-                    const uint8_t* a1 = a0 + (size_t)p.KS * 4 * 512;   // next weight block
-                    bulk_load_hint(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE, a0, 2048, sb, pol_stream);
-                    bulk_load_hint(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE + 2048, a1, 2048, sb,
-                                   pol_stream);
+                } else if (role == 0) {
                     if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * Cfg::W_TILE);
                     tma_load_2d_pair(base + Cfg::OFF_W + s * Cfg::W_TILE, &tm_w, fl, 0,
                                      wrow + 128 * ks);
-                } else {
-                    mbar_arrive_expect_tx(sb, Cfg::TSF_STAGE);
-                    tma_load_3d(base + Cfg::OFF_TSF + s * Cfg::TSF_STAGE, &p.tm_asf[7], sb, ks * 16,
-                                trow, tc.g);
+                } else if (role == 1) {
                     if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * Cfg::T_TILE);
                     tma_load_3d_pair(base + Cfg::OFF_T + s * Cfg::T_TILE, &p.tm_a[7], fl, ks * 128,
                                      trow, tc.g);
+                } else {
+                    // the peer's empty barrier completed with this one (same
+                    // multicast commit), so its slot s is free as well
+                    const uint32_t sb = bar_sfull + 8 * s;
+                    mbar_arrive_expect_tx(sb, Cfg::WSF_STAGE + Cfg::TSF_STAGE);
+                    bulk_load_multicast(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE + rank * 2048,
+                                        p.wsf + (wsf0 + 4 * (size_t)ks) * 512, 2048, sb, 0x3);
+                    tma_load_3d(base + Cfg::OFF_TSF + s * Cfg::TSF_STAGE, &p.tm_asf[7], sb, ks * 16,
+                                trow, tc.g);
                 }
                 __syncwarp();
                 ++issued;
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
         }
-        // Drain: this CTA's scale copies, and (leader) every operand copy of
-        // both CTAs, must have landed before the CTAs may exit; the peer is
-        // kept alive by the final cluster barrier until the leader drained.
+        // Drain: this CTA's scale copies (its own and the peer's multicast
+        // atoms), and (leader) every operand copy of both CTAs, must have
+        // landed before the CTAs may exit; the final cluster barrier keeps
+        // both CTAs alive until then.
         for (int st = 0; st < STAGES; ++st) {
             if (st >= issued) break;
             const long long last = st + (long long)STAGES * ((issued - 1 - st) / STAGES);
             const uint32_t par = (uint32_t)((last / STAGES) & 1);
             volatile int no_abort = 0;
-            if (leader) wait_bounded(bar_full + 8 * st, par, &no_abort, p.err, p.timeout_ns);
-            wait_bounded(bar_sfull + 8 * st, par, &no_abort, p.err, p.timeout_ns);
+            if (role == 2) wait_bounded(bar_sfull + 8 * st, par, &no_abort, p.err, p.timeout_ns);
+            else if (leader) wait_bounded(bar_full + 8 * st, par, &no_abort, p.err, p.timeout_ns);
         }
     } else if (warp == 1 && leader) {
         // ---------------------------------------------------- MMA warp (leader)
@@ -344,7 +355,7 @@ gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams p,
                 if (++s == STAGES) { s = 0; ph ^= 1u; }
             }
         }
-    } else if (warp >= 7) {
+    } else if (warp >= 7 && warp <= 14) {
         // ------------------------------------------------------------ epilogue
         const int ew = warp - 7;          // 0..7
         const int quad = warp & 3;        // TMEM lane quarter this warp may access

@@ -252,7 +252,7 @@ int launch_tok_pair(DeviceState* d, int slot, const GemmParams& p, const CUtenso
     if (!d->attr_set[slot]) {
         if (cudaFuncSetAttribute(gemm_nt_masked_tok_pair_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 Cfg::SMEM_BYTES) != cudaSuccess)
+                                 Cfg::SMEM_LIMIT) != cudaSuccess)
             return NVFP4GG_ERR_CUDA;
         d->attr_set[slot] = true;
     }
@@ -262,7 +262,7 @@ int launch_tok_pair(DeviceState* d, int slot, const GemmParams& p, const CUtenso
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas, 1, 1);
     cfg.blockDim = dim3(kTokThreads, 1, 1);
-    cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+    cfg.dynamicSmemBytes = Cfg::smem_bytes(p.G);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -475,7 +475,7 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
     const bool pair_fits = g_sm_cap == 0 || g_sm_cap >= 2;
     const bool pairable = !narrow && !swiglu && !signals && N % 256 == 0 && pair_fits;
     // token-major pairs (256 x 256 MMA tiles) for compute-heavy experts
-    const bool tok = pairable && M_total == 0 && M_max >= 128 &&
+    const bool tok = pairable && M_total == 0 && M_max >= 128 && G <= TokPairCfg::MAX_GROUPS &&
                      (g_pair_mode == 3 || (g_pair_mode == 2 && M_max > kPairAutoMaxRows));
     const bool pair = pairable && !tok &&
                       (g_pair_mode == 1 || (g_pair_mode == 2 && M_max <= kPairAutoMaxRows));
