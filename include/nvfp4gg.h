@@ -127,8 +127,11 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
  *   split_k    1..16, or 0 to choose from the tile count: floor(SMs / tiles),
  *              at most K/256 and 16
  *   workspace  device scratch owned by the caller, 256-byte aligned, at least
- *              nvfp4_splitk_workspace_bytes(G, M_max, N, K, split_k) bytes;
- *              calls that run at the same time must not share it
+ *              nvfp4_splitk_workspace_bytes(G, M_max, N, K, split_k) bytes
+ *              (fp32 partials, then one 8-byte arrival counter per tile);
+ *              it needs no initial value and no clearing between calls (the
+ *              counters are tagged with a number unique to each call); calls
+ *              that run at the same time must not share it
  * Other arguments as in nvfp4_grouped_gemm_nt_masked.  With M_max > 64 the
  * call runs unsplit and the workspace is not touched.  Results agree with the
  * unsplit call up to fp32 summation order.
@@ -151,7 +154,7 @@ int nvfp4_grouped_gemm_nt_masked_splitk(const void* A, const void* A_sf, const v
  * is a static __device__ array of the library, reserved once per device when
  * the library's module is loaded there:
  *   NVFP4GG_NOALLOC_MAX_SLOTS fp32 partial tiles of 32 x 128 (16 KiB each,
- *   4 MiB in all) plus one int arrival counter per slot (1 KiB).
+ *   4 MiB in all) plus one 8-byte arrival counter per slot (2 KiB).
  * A split call uses tiles x split slots, tiles = G * ceil(M_max/32) *
  * ceil(N/128) (every expert counted full).
  *   split_k  0: the automatic split of the workspace variant, lowered until
@@ -163,11 +166,12 @@ int nvfp4_grouped_gemm_nt_masked_splitk(const void* A, const void* A_sf, const v
  *               NVFP4GG_NOALLOC_MAX_SLOTS.
  * With M_max > 64 the call runs unsplit.  Other arguments as in
  * nvfp4_grouped_gemm_nt_masked.
- * State: the partials need no initial value; the counters must be zero when
- * a split kernel starts.  They are zero when the module loads, and each call
- * clears the ones it uses with an asynchronous memset on `stream` before its
- * launch; after a call that completed without a device-side timeout they
- * are zero again.
+ * State: neither the partials nor the counters need an initial value or
+ * clearing between calls: every call tags the counters it uses with a
+ * number unique to the call (the first arrival of a call restarts a counter
+ * that holds another call's number), so a call that ended in a device-side
+ * timeout leaves nothing for the next call to clean up.  Nothing besides
+ * the GEMM kernel is launched.
  * The first call on a device looks up the scratch's device address
  * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit: make one
  * call on each device before capturing a stream.
@@ -237,9 +241,9 @@ int nvfp4_grouped_gemm_nt_contiguous(const void* A, const void* A_sf, const void
  *                acquire ordering (or fence) before reading it.
  * Other arguments as in nvfp4_grouped_gemm_nt_masked; runs on the single-CTA
  * kernels.  The per-expert counters behind the signals are a static array of
- * the library (NVFP4GG_MAX_GROUPS ints per device), cleared on `stream`
- * before each call: calls of this entry point that overlap on one device
- * race on them.
+ * the library (NVFP4GG_MAX_GROUPS 8-byte counters per device), tagged with
+ * a number unique to each call (no clearing between calls): calls of this
+ * entry point that overlap on one device race on them.
  */
 int nvfp4_grouped_gemm_nt_masked_signals(const void* A, const void* A_sf, const void* B,
                                          const void* B_sf, const float* alpha, const int* masked_m,

@@ -74,12 +74,15 @@ struct GemmParams {
     // the last range to finish (counter ws_cnt[tile]) sums them in range order
     int split;
     float* ws_part;
-    int* ws_cnt;
+    unsigned long long* ws_cnt;
     // per-expert completion signals (null: none): signals[g] is incremented
     // once per call after all of expert g's valid rows of C are stored;
-    // sig_cnt[G] counts finished tile parts (zero at kernel start)
+    // sig_cnt[G] counts finished tile parts
     int* signals;
-    int* sig_cnt;
+    unsigned long long* sig_cnt;
+    // a number unique to this call (never 0): arrival counters are tagged
+    // with it, so they need no clearing between calls (epoch_arrive)
+    unsigned long long epoch;
     // packed-rows layout (contiguous != 0): A, A_sf and C hold only valid
     // rows, expert g's from row off[g] = sum_{h<g} masked_m[h], M_total rows
     // in all; token tensor maps are over [M_total] rows with one group
@@ -196,18 +199,36 @@ struct TileCoord {
 template <int TT_MAX>
 __device__ __forceinline__ int token_tiles(int m);
 
+// Arrival on a counter shared by the CTAs of one call, without clearing it
+// between calls: the counter holds epoch * span + arrivals, and the first
+// arrival of a call finds another epoch's value (an earlier call's, or
+// whatever the memory held) and restarts the count.  Returns this arrival's
+// number (1-based).  A lock-free CAS loop: a retry means another arrival
+// succeeded, and a call has at most `span` - 1 arrivals per counter.
+__device__ __forceinline__ unsigned long long epoch_arrive(unsigned long long* c,
+                                                           unsigned long long epoch,
+                                                           unsigned long long span) {
+    const unsigned long long base = epoch * span;
+    unsigned long long seen = *reinterpret_cast<volatile unsigned long long*>(c);
+    for (;;) {
+        const unsigned long long next = (seen >= base && seen - base < span) ? seen + 1 : base + 1;
+        const unsigned long long prev = atomicCAS(c, seen, next);
+        if (prev == seen) return next - base;
+        seen = prev;
+    }
+}
+
 // After one epilogue warp stored its part of a tile of expert tc.g: count the
-// part; the last of the expert's 4 x (tiles) parts resets the count and
-// increments the expert's signal.  Each lane fences its own stores first.
+// part; the last of the expert's 4 x (tiles) parts increments the expert's
+// signal.  Each lane fences its own stores first.
 template <int TT_MAX>
 __device__ __forceinline__ void signal_tile_part(const GemmParams& p, const TileCoord& tc, int lane) {
     if (!p.signals) return;
     __threadfence();
     __syncwarp();
     if (lane == 0) {
-        const int parts = 4 * token_tiles<TT_MAX>(tc.m) * p.NT;
-        if (atomicAdd(p.sig_cnt + tc.g, 1) == parts - 1) {
-            p.sig_cnt[tc.g] = 0;
+        const unsigned long long parts = 4ull * token_tiles<TT_MAX>(tc.m) * p.NT;
+        if (epoch_arrive(p.sig_cnt + tc.g, p.epoch, 1ull << 32) == parts) {
             __threadfence();
             atomicAdd(p.signals + tc.g, 1);
         }
@@ -675,7 +696,8 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                 if (ew == 0 && lane == 0) {
                     const int stop = *abort_flag;
                     *epi_stop = stop;
-                    *epi_flag = (!stop && atomicAdd(p.ws_cnt + tile, 1) == p.split - 1) ? 1 : 0;
+                    *epi_flag = (!stop && epoch_arrive(p.ws_cnt + tile, p.epoch, 64) ==
+                                              (unsigned long long)p.split) ? 1 : 0;
                 }
                 named_barrier_sync(1, 128);
                 if (*epi_flag) {
@@ -704,7 +726,6 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                         }
                         __syncwarp();
                     }
-                    if (ew == 0 && lane == 0) p.ws_cnt[tile] = 0;   // ready for the next call
                 }
                 const bool stop = *epi_stop != 0;
                 named_barrier_sync(1, 128);   // epi_flag / epi_stop are reused by the next unit

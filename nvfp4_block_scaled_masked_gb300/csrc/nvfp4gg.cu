@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -18,8 +19,9 @@ using namespace nvfp4gg;
 
 // Device error word (one per device that loads the library).
 static __device__ int g_error_word;
-// Per-expert tile-part counters of the completion-signal entry point.
-static __device__ int g_signal_counts[NVFP4GG_MAX_GROUPS];
+// Per-expert tile-part counters of the completion-signal entry point
+// (epoch-tagged: see epoch_arrive).
+static __device__ unsigned long long g_signal_counts[NVFP4GG_MAX_GROUPS];
 
 namespace {
 
@@ -39,6 +41,8 @@ int g_sm_cap = 0;
 int g_pair_mode = 2;   // prefill kernel family: 0 single, 1 pairs, 2 automatic, 3 token-major pairs (nvfp4gg.h)
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 unsigned long long g_timeout_ns = 2000000000ull;   // 2 s per device-side wait
+// Call numbers for the epoch-tagged arrival counters (split-K, signals).
+std::atomic<unsigned long long> g_epoch{0};
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? NVFP4GG_OK : NVFP4GG_ERR_CUDA; }
 
@@ -425,15 +429,15 @@ long long decode_tile_bound(int G, int M_max, int N) {
 }
 
 // Device address of this device's signal counters (looked up once per device).
-int* g_signal_addr[kMaxDevices] = {};
-int signal_counts(int** out) {
+unsigned long long* g_signal_addr[kMaxDevices] = {};
+int signal_counts(unsigned long long** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4GG_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_signal_addr[dev]) {
         void* ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_signal_counts) != cudaSuccess || !ptr) return NVFP4GG_ERR_CUDA;
-        g_signal_addr[dev] = static_cast<int*>(ptr);
+        g_signal_addr[dev] = static_cast<unsigned long long*>(ptr);
     }
     *out = g_signal_addr[dev];
     return NVFP4GG_OK;
@@ -454,7 +458,7 @@ int auto_split(DeviceState* d, long long tiles, int K) {
 
 int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf, const float* alpha,
                 const int* masked_m, void* C, int G, int M_max, int N, int K, int split,
-                float* ws_part, int* ws_cnt, void* stream, bool swiglu = false,
+                float* ws_part, unsigned long long* ws_cnt, void* stream, bool swiglu = false,
                 int* signals = nullptr, int M_total = 0, uint8_t* qa = nullptr,
                 uint8_t* qsf = nullptr, const float* qscale = nullptr) {
     // with the NVFP4 output of the SwiGLU epilogue (qa), C may be null
@@ -505,21 +509,18 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
     p.KS = K / 256;
     p.timeout_ns = g_timeout_ns;
     p.split = 1;
+    p.epoch = ++g_epoch;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (narrow && split > 1) {
         const long long tiles = decode_tile_bound(G, M_max, N);
         if (tiles * split >= (1LL << 31)) return NVFP4GG_ERR_SHAPE;
-        if (cudaMemsetAsync(ws_cnt, 0, (size_t)tiles * sizeof(int), st) != cudaSuccess)
-            return NVFP4GG_ERR_CUDA;
         p.split = split;
         p.ws_part = ws_part;
         p.ws_cnt = ws_cnt;
     }
     if (signals) {
-        int* counts = nullptr;
+        unsigned long long* counts = nullptr;
         if ((rc = signal_counts(&counts)) != NVFP4GG_OK) return rc;
-        if (cudaMemsetAsync(counts, 0, (size_t)G * sizeof(int), st) != cudaSuccess)
-            return NVFP4GG_ERR_CUDA;
         p.signals = signals;
         p.sig_cnt = counts;
     }
@@ -674,7 +675,7 @@ size_t nvfp4_splitk_workspace_bytes(int G, int M_max, int N, int K, int split_k)
     if (M_max > 64) return 16;   // prefill shapes run unsplit: no workspace needed
     const long long tiles = decode_tile_bound(G, M_max, N);
     const int s = split_k == 0 ? 16 : split_k;
-    return ((splitk_part_bytes(tiles, s) + 255) & ~(size_t)255) + (size_t)tiles * sizeof(int);
+    return ((splitk_part_bytes(tiles, s) + 255) & ~(size_t)255) + (size_t)tiles * 8;
 }
 
 int nvfp4_grouped_gemm_nt_masked_splitk(const void* A, const void* A_sf, const void* B,
@@ -699,9 +700,10 @@ int nvfp4_grouped_gemm_nt_masked_splitk(const void* A, const void* A_sf, const v
     if (split < 1) split = 1;
     const long long tiles = decode_tile_bound(G, M_max, N);
     const size_t part = (splitk_part_bytes(tiles, split) + 255) & ~(size_t)255;
-    if (workspace_bytes < part + (size_t)tiles * sizeof(int)) return NVFP4GG_ERR_SHAPE;
+    if (workspace_bytes < part + (size_t)tiles * 8) return NVFP4GG_ERR_SHAPE;
     float* ws_part = static_cast<float*>(workspace);
-    int* ws_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + part);
+    unsigned long long* ws_cnt =
+        reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(workspace) + part);
     return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, split, ws_part, ws_cnt,
                        stream);
 }
@@ -891,7 +893,7 @@ namespace {
 
 constexpr size_t kNoAllocPartBytes =
     (size_t)NVFP4GG_NOALLOC_MAX_SLOTS * kNarrowTT * 128 * sizeof(float);   // 4 MiB
-constexpr size_t kNoAllocBytes = kNoAllocPartBytes + NVFP4GG_NOALLOC_MAX_SLOTS * sizeof(int);
+constexpr size_t kNoAllocBytes = kNoAllocPartBytes + NVFP4GG_NOALLOC_MAX_SLOTS * 8;
 static_assert(kNoAllocPartBytes % 256 == 0, "counters must start 256-byte aligned");
 
 }  // namespace
@@ -950,5 +952,5 @@ extern "C" int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(
     if ((rc = noalloc_scratch(&scratch)) != NVFP4GG_OK) return rc;
     return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, split,
                        reinterpret_cast<float*>(scratch),
-                       reinterpret_cast<int*>(scratch + kNoAllocPartBytes), stream);
+                       reinterpret_cast<unsigned long long*>(scratch + kNoAllocPartBytes), stream);
 }

@@ -106,7 +106,7 @@ def test_splitk_argument_checks(lib):
     f = lib.nvfp4_grouped_gemm_nt_masked_splitk
     need = binding.nvfp4_splitk_workspace_bytes(4, 16, 256, 512, 2)
     tiles = 4 * 1 * 2
-    assert need == (tiles * 2 * 32 * 128 * 4 + 255) // 256 * 256 + tiles * 4
+    assert need == (tiles * 2 * 32 * 128 * 4 + 255) // 256 * 256 + tiles * 8
     assert binding.nvfp4_splitk_workspace_bytes(4, 16, 256, 512, 17) == 0
     args = [FAKE] * 7 + [4, 16, 256, 512, 2, FAKE, need, None]
     a = list(args); a[12] = None

@@ -174,7 +174,9 @@ def run_gpu_splitk(d, split_k):
     cfg = d["cfg"]
     prob = Problem(d)
     nbytes = binding.nvfp4_splitk_workspace_bytes(cfg.G, cfg.M_max, cfg.N, cfg.K, split_k)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    # the workspace needs no initial value: arbitrary bytes in it (counters
+    # included) must not change the result
+    ws = torch.randint(0, 256, (nbytes,), dtype=torch.uint8, device="cuda")
     outs = []
     for _ in range(2):      # deterministic: two calls give the same bits
         prob.reset_C()
