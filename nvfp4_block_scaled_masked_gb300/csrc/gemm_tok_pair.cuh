@@ -87,7 +87,12 @@ struct TokPairCfg {
 };
 
 // Tile id -> (expert, weight-block pair, first token of the 256, masked_m).
-__device__ __forceinline__ TileCoord decode_tok_tile(const int* cum, const int* gm, int G,
+// Within an expert the weight-block pair runs fastest: the CTAs working at
+// one time then share one or two token tiles and cycle through all of the
+// expert's weights, which stay in L2 for its next token tiles (with the
+// token tile fastest, every round of tiles would start on weights that no
+// CTA has read yet, all fetched from DRAM at the same moment).
+__device__ __forceinline__ TileCoord decode_tok_tile(const int* cum, const int* gm, int G, int NP,
                                                      int tile) {
     int lo = 0, hi = G - 1;
     while (lo < hi) {
@@ -98,10 +103,10 @@ __device__ __forceinline__ TileCoord decode_tok_tile(const int* cum, const int* 
     c.g = lo;
     c.m = gm[lo];
     const int local = tile - cum[lo];
-    const int ntt = (c.m + 255) >> 8;
+    const int tt = local / NP;
     c.w = 256;
-    c.nt = local / ntt;              // weight-block pair
-    c.t0 = (local - c.nt * ntt) * 256;
+    c.nt = local - tt * NP;          // weight-block pair
+    c.t0 = tt * 256;
     return c;
 }
 
@@ -210,7 +215,7 @@ gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams p,
         long long issued = 0;
         bool ok = true;
         for (int tile = cid; tile < total && ok; tile += ncl) {
-            const TileCoord tc = decode_tok_tile(cum, gm, p.G, tile);
+            const TileCoord tc = decode_tok_tile(cum, gm, p.G, NP, tile);
             const int nt = 2 * tc.nt + (int)rank;                // this CTA's weight block
             const size_t wsf0 = ((size_t)tc.g * p.NT + nt) * (size_t)(p.KS * 4);   // atom index
             // row of this CTA's weight tile in the prepared-tile map, stage 0
@@ -364,24 +369,33 @@ gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams p,
         uint8_t* stage = sbase + Cfg::OFF_EPI + ew * Cfg::EPI_WARP_BYTES;
         uint32_t aph = 0;
         for (int tile = cid; tile < total; tile += ncl) {
-            const TileCoord tc = decode_tok_tile(cum, gm, p.G, tile);
+            const TileCoord tc = decode_tok_tile(cum, gm, p.G, NP, tile);
             const bool ok = __all_sync(0xffffffffu, wait_bounded(bar_accf, aph, abort_flag, p.err,
                                                                  p.timeout_ns));
             if (!ok) break;
             tc_fence_after();
             const float al = __ldg(p.alpha + tc.g);
             const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + 128 * half;
-            // the whole accumulator quarter-half into registers as bf16 pairs
+            // the whole accumulator quarter-half into registers as bf16 pairs,
+            // in 16-column loads, each issued before the previous one is
+            // converted (the conversion overlaps the next load's latency)
             uint32_t o[64];
+            uint32_t ra[16], rb[16];
+            tmem_ld_32x32b_x16(tbase, ra);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tbase + 32 * c, r);
-                tmem_wait_ld();
+            for (int c = 0; c < 8; c += 2) {
+                tmem_wait_ld_regs(ra);
+                tmem_ld_32x32b_x16(tbase + 16 * (c + 1), rb);
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    o[16 * c + j] = pack_bf16x2(al * __uint_as_float(r[2 * j]),
-                                                al * __uint_as_float(r[2 * j + 1]));
+                for (int j = 0; j < 8; ++j)
+                    o[8 * c + j] = pack_bf16x2(al * __uint_as_float(ra[2 * j]),
+                                               al * __uint_as_float(ra[2 * j + 1]));
+                tmem_wait_ld_regs(rb);
+                if (c + 2 < 8) tmem_ld_32x32b_x16(tbase + 16 * (c + 2), ra);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    o[8 * (c + 1) + j] = pack_bf16x2(al * __uint_as_float(rb[2 * j]),
+                                                     al * __uint_as_float(rb[2 * j + 1]));
             }
             // TMEM is free: the next tile's MMAs may start while this warp
             // stores (the stores overlap that tile's main loop)

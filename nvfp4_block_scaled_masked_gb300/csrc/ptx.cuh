@@ -430,6 +430,18 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
         : "memory");
 }
 
+// tcgen05.wait::ld that names the 16 destination registers of the load it
+// waits for as operands, so that the compiler cannot move their uses above
+// the wait while the load is in flight.
+__device__ __forceinline__ void tmem_wait_ld_regs(uint32_t (&r)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15])
+                 :
+                 : "memory");
+}
+
 // Two fp32 values to one packed bf16x2 word (round to nearest even); `lo`
 // lands in the low half (the lower address).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
