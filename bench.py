@@ -399,6 +399,7 @@ def main():
         e1.synchronize()
         prep_ms.append(e0.elapsed_time(e1))
     prob.raw_B = prob.raw_Bsf = None
+    torch.cuda.empty_cache()   # the device then holds only what the timed call uses
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     if args.splitk >= 0:
