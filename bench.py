@@ -532,6 +532,9 @@ def main():
                             "frac": gbs / peaks["hbm"], "traffic": profiled_traffic(cfg.key),
                             "algorithmic_bytes": counts["bytes"],
                             "peak_note": f"HBM copy bandwidth, {peaks['src']}"}
+    if args.splitk >= 0 or args.swiglu:
+        # the recorded DRAM traffic is the plain GEMM kernel's, not this entry point's
+        line["roofline"]["traffic"] = None
     kept = {}
     if args.per_config_steps > 0 and ws == 1:
         plain = args.splitk < 0 and not args.swiglu
