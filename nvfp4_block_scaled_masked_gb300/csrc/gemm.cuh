@@ -114,18 +114,28 @@ __host__ __device__ constexpr int pow2_cols(int n) {
     return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : n <= 256 ? 256 : 512;
 }
 
-template <int TT_MAX, int STAGES>
+// A ring stage holds KSUB K-tiles of 256 codes.  Every stage costs a fixed
+// few hundred nanoseconds of barrier hand-offs (producer, scale warps, MMA
+// warp) whatever its size, so when few CTAs share the weight stream the
+// bytes per stage set each SM's share of it: two K-tiles per stage move
+// twice the bytes per hand-off.
+template <int TT_MAX, int STAGES, int KSUB = 1>
 struct KCfg {
     static_assert(TT_MAX % 32 == 0 && TT_MAX <= 256, "token tile");
-    static_assert(STAGES >= 3, "ring depth");
-    static constexpr int W_TILE = 128 * 128;         // 128 weight rows x 256 codes
-    static constexpr int T_TILE = TT_MAX * 128;      // TT_MAX token rows x 256 codes
-    static constexpr int WSF_STAGE = 4 * 512;        // 4 weight-scale atoms
-    static constexpr int TSF_PLAIN = TT_MAX * 16;    // token scales, 16 bytes per row
+    static_assert(STAGES >= 3 || (KSUB > 1 && STAGES >= 2), "ring depth");
+    static_assert(KSUB == 1 || KSUB == 2, "K-tiles per stage");
+    static constexpr int W_TILE = 128 * 128;         // one K-tile: 128 weight rows x 256 codes
+    static constexpr int T_TILE = TT_MAX * 128;      // one K-tile: TT_MAX token rows x 256 codes
+    static constexpr int WSF_TILE = 4 * 512;         // one K-tile: 4 weight-scale atoms
+    static constexpr int TSF_PLAIN = TT_MAX * 16;    // one K-tile: token scales, 16 bytes per row
+    static constexpr int W_STAGE = KSUB * W_TILE;
+    static constexpr int T_STAGE = KSUB * T_TILE;
+    static constexpr int WSF_STAGE = KSUB * WSF_TILE;
+    static constexpr int TSF_STAGE = KSUB * TSF_PLAIN;
     static constexpr int NA = (TT_MAX + 127) / 128;  // 128-row token groups per MMA
     static constexpr int ACC_BUFS = 2;
-    static constexpr int SFW_COLS = 16;              // 4 MMAs x 4 columns
-    static constexpr int SFT_COLS = 16 * NA;
+    static constexpr int SFW_COLS = 16 * KSUB;       // 4 MMAs x 4 columns per K-tile
+    static constexpr int SFT_COLS = 16 * NA * KSUB;
     static constexpr int SF_COLS = SFW_COLS + SFT_COLS;
     // Scale-factor TMEM regions, used round-robin by stage count.  With one
     // region per ring stage a region is rewritten only after the stage's next
@@ -143,10 +153,10 @@ struct KCfg {
     static constexpr int TMEM_COLS = pow2_cols(TMEM_NEED);
 
     static constexpr int OFF_W = 0;
-    static constexpr int OFF_T = OFF_W + STAGES * W_TILE;
-    static constexpr int OFF_WSF = OFF_T + STAGES * T_TILE;
+    static constexpr int OFF_T = OFF_W + STAGES * W_STAGE;
+    static constexpr int OFF_WSF = OFF_T + STAGES * T_STAGE;
     static constexpr int OFF_TSFP = OFF_WSF + STAGES * WSF_STAGE;
-    static constexpr int OFF_EPI = OFF_TSFP + STAGES * TSF_PLAIN;   // 4 warps x 16 tokens x 32 n bf16
+    static constexpr int OFF_EPI = OFF_TSFP + STAGES * TSF_STAGE;   // 4 warps x 16 tokens x 32 n bf16
     static constexpr int EPI_BYTES = 4 * 16 * 32 * 2;
     static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
     // full, sfull, empty, sfready per stage; acc full/empty per buffer; MMA drain
@@ -158,6 +168,7 @@ struct KCfg {
     static constexpr int TAB_BYTES = (3 * kGroupsMax + 2) * 4;
     static constexpr int SMEM_BYTES = OFF_TAB + TAB_BYTES + 1024;   // + alignment slack
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+    static_assert(OFF_T % 1024 == 0 && T_TILE % 1024 == 0, "128-byte swizzle alignment");
 };
 
 // Barrier among `threads` threads (whole warps) on hardware barrier `id`.
@@ -268,10 +279,13 @@ __device__ __forceinline__ TileCoord decode_tile(const int* cum, const int* gm, 
 // up rows of the same 16 output columns.  Lane l < 16 then combines its
 // h_gate = alpha * acc with lane l + 16's h_up into silu(h_gate) * h_up, and
 // C is bf16 [G][M_max][N/2], output column = 64 * block + 16 * quarter + l.
-template <int TT_MAX, int STAGES, bool SWIGLU = false>
+template <int TT_MAX, int STAGES, bool SWIGLU = false, int KSUB = 1>
 __global__ void __launch_bounds__(kThreads, 1)
 gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
-    using Cfg = KCfg<TT_MAX, STAGES>;
+    using Cfg = KCfg<TT_MAX, STAGES, KSUB>;
+    // ring stages per tile: K-tiles of 256 codes, KSUB per stage (the host
+    // picks KSUB = 2 only where it divides K / 256)
+    const int KSS = p.KS / KSUB;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -392,11 +406,11 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const int tile = u / p.split;
             int kb, ke;
-            k_range(u - tile * p.split, p.split, p.KS, kb, ke);
+            k_range(u - tile * p.split, p.split, KSS, kb, ke);
             const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
             const size_t wtile = ((size_t)tc.g * p.NT + tc.nt) * (size_t)p.KS;
             const uint8_t* wq_tile = p.wq + wtile * Cfg::W_TILE;
-            const uint8_t* wsf_tile = p.wsf + wtile * Cfg::WSF_STAGE;
+            const uint8_t* wsf_tile = p.wsf + wtile * Cfg::WSF_TILE;
             const int box = (tc.w >> 4) - 1;   // tensor map of this token width
             for (int ks = kb; ks < ke; ++ks) {
                 ok = __all_sync(0xffffffffu, wait_bounded(bar_empty + 8 * s, ph ^ 1u, abort_flag,
@@ -406,24 +420,30 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                 // operand tiles are still in flight), then the operand tile
                 const uint32_t fb = bar_full + 8 * s;
                 const uint32_t sb = bar_sfull + 8 * s;
+                // (the stage's KSUB K-tiles of weights and of their scale
+                // atoms are contiguous in the prepared layout: one copy each)
                 if (!elect_one()) {
                 } else if (weights) {
                     mbar_arrive_expect_tx(sb, Cfg::WSF_STAGE);
                     bulk_load_hint(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE,
                                    wsf_tile + (size_t)ks * Cfg::WSF_STAGE, Cfg::WSF_STAGE, sb,
                                    pol_stream);
-                    mbar_arrive_expect_tx(fb, Cfg::W_TILE);
-                    bulk_load_hint(base + Cfg::OFF_W + s * Cfg::W_TILE,
-                                   wq_tile + (size_t)ks * Cfg::W_TILE, Cfg::W_TILE, fb, pol_stream);
+                    mbar_arrive_expect_tx(fb, Cfg::W_STAGE);
+                    bulk_load_hint(base + Cfg::OFF_W + s * Cfg::W_STAGE,
+                                   wq_tile + (size_t)ks * Cfg::W_STAGE, Cfg::W_STAGE, fb, pol_stream);
                 } else {
-                    mbar_arrive_expect_tx(sb, tc.w * 16);
+                    mbar_arrive_expect_tx(sb, tc.w * 16 * KSUB);
+                    mbar_arrive_expect_tx(fb, tc.w * 128 * KSUB);
                     const int ty = p.contiguous ? off[tc.g] + tc.t0 : tc.t0;
                     const int tz = p.contiguous ? 0 : tc.g;
-                    tma_load_3d(base + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN, &p.tm_asf[box], sb,
-                                ks * 16, ty, tz);
-                    mbar_arrive_expect_tx(fb, tc.w * 128);
-                    tma_load_3d(base + Cfg::OFF_T + s * Cfg::T_TILE, &p.tm_a[box], fb, ks * 128,
-                                ty, tz);
+#pragma unroll
+                    for (int i = 0; i < KSUB; ++i) {
+                        const int kt = ks * KSUB + i;   // K-tile
+                        tma_load_3d(base + Cfg::OFF_TSFP + s * Cfg::TSF_STAGE + i * Cfg::TSF_PLAIN,
+                                    &p.tm_asf[box], sb, kt * 16, ty, tz);
+                        tma_load_3d(base + Cfg::OFF_T + s * Cfg::T_STAGE + i * Cfg::T_TILE,
+                                    &p.tm_a[box], fb, kt * 128, ty, tz);
+                    }
                 }
                 __syncwarp();
                 ++issued;
@@ -453,7 +473,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const int tile = u / p.split;
             int kb, ke;
-            k_range(u - tile * p.split, p.split, p.KS, kb, ke);
+            k_range(u - tile * p.split, p.split, KSS, kb, ke);
             const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
             ok = __all_sync(0xffffffffu, wait_bounded(bar_acce + 8 * acc, aph ^ 1u, abort_flag,
                                                       p.err, p.timeout_ns));
@@ -469,16 +489,25 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                                                           p.err, p.timeout_ns));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t sfw = tmem_sf + r * Cfg::SF_COLS;
-                const uint32_t sft = sfw + Cfg::SFW_COLS;
-                const uint64_t ad = sdesc_k_sw128(base + Cfg::OFF_W + s * Cfg::W_TILE);
-                const uint64_t bd = sdesc_k_sw128(base + Cfg::OFF_T + s * Cfg::T_TILE);
-                const uint32_t acc_in = ks != kb;
+                const uint32_t sfw0 = tmem_sf + r * Cfg::SF_COLS;
+                const uint32_t sft0 = sfw0 + Cfg::SFW_COLS;
                 if (elect_one()) {
-                    umma_mxf4nvf4(d_tmem, ad, bd, idesc, sfw, sft, acc_in);
-                    umma_mxf4nvf4(d_tmem, ad + 2, bd + 2, idesc, sfw + 4, sft + 4 * Cfg::NA, 1u);
-                    umma_mxf4nvf4(d_tmem, ad + 4, bd + 4, idesc, sfw + 8, sft + 8 * Cfg::NA, 1u);
-                    umma_mxf4nvf4(d_tmem, ad + 6, bd + 6, idesc, sfw + 12, sft + 12 * Cfg::NA, 1u);
+#pragma unroll
+                    for (int i = 0; i < KSUB; ++i) {
+                        // K-tile i of the stage: its operand tiles, 16 weight-
+                        // and 16 NA token-scale columns
+                        const uint64_t ad =
+                            sdesc_k_sw128(base + Cfg::OFF_W + s * Cfg::W_STAGE + i * Cfg::W_TILE);
+                        const uint64_t bd =
+                            sdesc_k_sw128(base + Cfg::OFF_T + s * Cfg::T_STAGE + i * Cfg::T_TILE);
+                        const uint32_t sfw = sfw0 + 16 * i;
+                        const uint32_t sft = sft0 + 16 * Cfg::NA * i;
+                        const uint32_t acc_in = (ks != kb || i > 0) ? 1u : 0u;
+                        umma_mxf4nvf4(d_tmem, ad, bd, idesc, sfw, sft, acc_in);
+                        umma_mxf4nvf4(d_tmem, ad + 2, bd + 2, idesc, sfw + 4, sft + 4 * Cfg::NA, 1u);
+                        umma_mxf4nvf4(d_tmem, ad + 4, bd + 4, idesc, sfw + 8, sft + 8 * Cfg::NA, 1u);
+                        umma_mxf4nvf4(d_tmem, ad + 6, bd + 6, idesc, sfw + 12, sft + 12 * Cfg::NA, 1u);
+                    }
                     umma_commit(bar_empty + 8 * s);
                     if (ks == ke - 1) umma_commit(bar_accf + 8 * acc);
                 }
@@ -504,7 +533,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
             const int tile = u / p.split;
             int kb, ke;
-            k_range(u - tile * p.split, p.split, p.KS, kb, ke);
+            k_range(u - tile * p.split, p.split, KSS, kb, ke);
             for (int ks = kb; ks < ke; ++ks) {
                 ok = __all_sync(0xffffffffu, wait_bounded(bar_sfull + 8 * s, ph, abort_flag,
                                                           p.err, p.timeout_ns));
@@ -522,39 +551,47 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                 // scale columns in the previous round completed before its
                 // loads were issued: empty barrier.)
                 tc_fence_after();
-                // weights: column 4q + c = word c of row `lane` of atom q
-                const uint8_t* wsf = sbase + Cfg::OFF_WSF + s * Cfg::WSF_STAGE + lane * 16;
-                uint32_t w[16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(wsf + 512 * q);
-                    w[4 * q] = v.x;
-                    w[4 * q + 1] = v.y;
-                    w[4 * q + 2] = v.z;
-                    w[4 * q + 3] = v.w;
-                }
-                // tokens: column 4(q NA + a) + c = word q of plain row
-                // 128a + 32c + lane (rows past TT_MAX: zero, never read)
-                const uint8_t* plain = sbase + Cfg::OFF_TSFP + s * Cfg::TSF_PLAIN + lane * 16;
-                uint32_t t[16 * Cfg::NA];
+                for (int i = 0; i < KSUB; ++i) {
+                    // K-tile i of the stage.  Weights: column 4q + c = word c
+                    // of row `lane` of atom q
+                    const uint8_t* wsf = sbase + Cfg::OFF_WSF + s * Cfg::WSF_STAGE +
+                                         i * Cfg::WSF_TILE + lane * 16;
+                    uint32_t w[16];
 #pragma unroll
-                for (int a = 0; a < Cfg::NA; ++a) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                        if (128 * a + 32 * c < TT_MAX)
-                            v = *reinterpret_cast<const uint4*>(plain + (128 * a + 32 * c) * 16);
-                        t[4 * (0 * Cfg::NA + a) + c] = v.x;
-                        t[4 * (1 * Cfg::NA + a) + c] = v.y;
-                        t[4 * (2 * Cfg::NA + a) + c] = v.z;
-                        t[4 * (3 * Cfg::NA + a) + c] = v.w;
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 v = *reinterpret_cast<const uint4*>(wsf + 512 * q);
+                        w[4 * q] = v.x;
+                        w[4 * q + 1] = v.y;
+                        w[4 * q + 2] = v.z;
+                        w[4 * q + 3] = v.w;
                     }
-                }
-                const uint32_t sfw = tmem_sf + r * Cfg::SF_COLS + lane_off;
-                tmem_st_32x32b_x16(sfw, w);
+                    // tokens: column 4(q NA + a) + c = word q of plain row
+                    // 128a + 32c + lane (rows past TT_MAX: zero, never read)
+                    const uint8_t* plain = sbase + Cfg::OFF_TSFP + s * Cfg::TSF_STAGE +
+                                           i * Cfg::TSF_PLAIN + lane * 16;
+                    uint32_t t[16 * Cfg::NA];
 #pragma unroll
-                for (int h = 0; h < Cfg::NA; ++h)
-                    tmem_st_32x32b_x16(sfw + Cfg::SFW_COLS + 16 * h, t + 16 * h);
+                    for (int a = 0; a < Cfg::NA; ++a) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                            if (128 * a + 32 * c < TT_MAX)
+                                v = *reinterpret_cast<const uint4*>(plain + (128 * a + 32 * c) * 16);
+                            t[4 * (0 * Cfg::NA + a) + c] = v.x;
+                            t[4 * (1 * Cfg::NA + a) + c] = v.y;
+                            t[4 * (2 * Cfg::NA + a) + c] = v.z;
+                            t[4 * (3 * Cfg::NA + a) + c] = v.w;
+                        }
+                    }
+                    const uint32_t sfw = tmem_sf + r * Cfg::SF_COLS + lane_off + 16 * i;
+                    const uint32_t sft = tmem_sf + r * Cfg::SF_COLS + lane_off + Cfg::SFW_COLS +
+                                         16 * Cfg::NA * i;
+                    tmem_st_32x32b_x16(sfw, w);
+#pragma unroll
+                    for (int h = 0; h < Cfg::NA; ++h)
+                        tmem_st_32x32b_x16(sft + 16 * h, t + 16 * h);
+                }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -691,27 +728,43 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(bar_acce + 8 * acc);   // TMEM no longer needed
                 }
-                __threadfence();
+                // the barrier orders the 4 warps' partial stores before the
+                // ticket; one device-scope fence by the ticket's thread then
+                // publishes them all (a fence in every thread waited for each
+                // thread's own stores to be acknowledged, microseconds per
+                // unit under a saturated memory system)
                 named_barrier_sync(1, 128);                          // the 4 epilogue warps
                 if (ew == 0 && lane == 0) {
                     const int stop = *abort_flag;
                     *epi_stop = stop;
+                    __threadfence();
                     *epi_flag = (!stop && epoch_arrive(p.ws_cnt + tile, p.epoch, 64) ==
                                               (unsigned long long)p.split) ? 1 : 0;
+                    __threadfence();   // acquire: the other ranges' partials, for the last range
                 }
                 named_barrier_sync(1, 128);
                 if (*epi_flag) {
                     // the last range: sum all ranges' partials in range order
-                    __threadfence();
                     const float* base_part = p.ws_part + (size_t)tile * p.split * (TT_MAX * 128) + quad * 32 + lane;
 #pragma unroll 1
                     for (int c = 0; c < TT_MAX / 16; ++c) {
                         if (c * 16 >= tc.w) break;
-#pragma unroll 4
+                        // every range's value of a column is loaded before
+                        // any is added (split <= 16), so the loads overlap
+                        // instead of each waiting for the previous sum; the
+                        // sum is still taken in range order
+#pragma unroll 2
                         for (int t = 0; t < 16; ++t) {
-                            float acc_v = 0.f;
-                            for (int r2 = 0; r2 < p.split; ++r2)
-                                acc_v += __ldcg(base_part + (size_t)r2 * (TT_MAX * 128) + (c * 16 + t) * 128);
+                            float v[16];
+#pragma unroll
+                            for (int r2 = 0; r2 < 16; ++r2)
+                                v[r2] = r2 < p.split ? __ldcg(base_part + (size_t)r2 * (TT_MAX * 128) +
+                                                              (c * 16 + t) * 128)
+                                                     : 0.f;
+                            float acc_v = v[0];
+#pragma unroll
+                            for (int r2 = 1; r2 < 16; ++r2)
+                                if (r2 < p.split) acc_v += v[r2];
                             sb[t * 32 + lane] = __float2bfloat16_rn(al * acc_v);
                         }
                         __syncwarp();

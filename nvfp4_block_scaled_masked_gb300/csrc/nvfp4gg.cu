@@ -32,7 +32,7 @@ struct DeviceState {
     int status = NVFP4GG_OK;
     int sms = 0;
     int* err = nullptr;          // device address of g_error_word
-    bool attr_set[8] = {};       // per kernel variant: max dynamic smem set
+    bool attr_set[12] = {};      // per kernel variant: max dynamic smem set
 };
 
 std::mutex g_mu;
@@ -165,10 +165,10 @@ int check_gemm_shape(int G, int M_max, int N, int K) {
     return NVFP4GG_OK;
 }
 
-template <int TT, int ST, bool SWIGLU = false>
+template <int TT, int ST, bool SWIGLU = false, int KSUB = 1>
 int launch_variant(DeviceState* d, int slot, const GemmParams& p, cudaStream_t stream) {
-    using Cfg = KCfg<TT, ST>;
-    auto kern = gemm_nt_masked_kernel<TT, ST, SWIGLU>;
+    using Cfg = KCfg<TT, ST, KSUB>;
+    auto kern = gemm_nt_masked_kernel<TT, ST, SWIGLU, KSUB>;
     if (!d->attr_set[slot]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::SMEM_BYTES) != cudaSuccess)
@@ -284,6 +284,8 @@ int launch_tok_pair(DeviceState* d, int slot, const GemmParams& p, const CUtenso
 // each MMA instruction carries 128 x 192 x 64 (the issuing warp's per-stage
 // cost, not the tensor pipe, bounds compute-heavy tiles).
 constexpr int kNarrowTT = 32, kNarrowStages = 8;
+// decode tiles with K % 512 == 0: stages of two K-tiles (same bytes in flight)
+constexpr int kNarrowStages2 = 4;
 constexpr int kWideTT = 192, kWideStages = 4;
 // Larger experts with N a multiple of 256: CTA pairs (M = 256 per MMA),
 // token tiles of up to 192 split 96 + 96 rows, six ring stages.
@@ -524,9 +526,16 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
         p.signals = signals;
         p.sig_cnt = counts;
     }
-    if (swiglu)
+    // decode tiles stream weights from few CTAs when there are few experts:
+    // two K-tiles per ring stage where K allows it (split-K ranges are then
+    // cut in stages: every range keeps at least one)
+    const bool ksub2 = narrow && p.KS % 2 == 0 && p.split * 2 <= p.KS;
+    if (swiglu) {
+        if (ksub2) return launch_variant<kNarrowTT, kNarrowStages2, true, 2>(d, 7, p, st);
         return narrow ? launch_variant<kNarrowTT, kNarrowStages, true>(d, 3, p, st)
                       : launch_variant<kWideTT, kWideStages, true>(d, 4, p, st);
+    }
+    if (ksub2) return launch_variant<kNarrowTT, kNarrowStages2, false, 2>(d, 6, p, st);
     if (narrow) return launch_variant<kNarrowTT, kNarrowStages>(d, 0, p, st);
     if (tok) {
         CUtensorMap tm_w;
