@@ -57,9 +57,8 @@ constexpr int kGroupsMax = NVFP4GG_MAX_GROUPS;
 constexpr int kThreads = 352;
 constexpr int kMaxWidths = 16;   // token tile widths 16, 32, ..., 256 rows
 
-struct GemmParams {
-    CUtensorMap tm_a[kMaxWidths];    // A codes u8 [G][M_max][K/2], box 128 x 16(i+1) rows, SW128
-    CUtensorMap tm_asf[kMaxWidths];  // A_sf u8 [G][M_max][K/16], box 16 x 16(i+1) rows
+// Scalar arguments of every GEMM kernel.
+struct GemmArgs {
     const uint8_t* wq;               // prepared codes: [G][NT][K/256][16384], pre-swizzled tiles
     const uint8_t* wsf;              // prepared scales: [G][NT][K/64][512]
     const float* alpha;
@@ -96,18 +95,36 @@ struct GemmParams {
     const float* qscale;
 };
 
+// Kernel parameters: the scalars and the token tensor maps of NW tile widths,
+// tm_a[i] / tm_asf[i] for 16 (i + 1) rows (the host picks which widths a
+// kernel variant can address).  Only these travel with a launch: a parameter
+// block of 32 maps (4 KB) was measured to add about a microsecond to every
+// call's launch.
+template <int NW>
+struct GemmParams : GemmArgs {
+    CUtensorMap tm_a[NW];    // A codes u8 [G][M_max][K/2], box 128 x rows, SW128
+    CUtensorMap tm_asf[NW];  // A_sf u8 [G][M_max][K/16], box 16 x rows
+};
+
 // Row of C holding token `tok` of expert g: g * M_max + tok in the masked
 // layout; off[g] + tok in the packed-rows layout, -1 past its M_total rows.
-__device__ __forceinline__ long long out_row(const GemmParams& p, const int* off, int g, int tok) {
+__device__ __forceinline__ long long out_row(const GemmArgs& p, const int* off, int g, int tok) {
     if (!p.contiguous) return (long long)g * p.M_max + tok;
     const int r = off[g] + tok;
     return r < p.M_total ? r : -1;
 }
 
-// K stages [kb, ke) of split range sp of S over KS stages (balanced).
+// K stages [kb, ke) of split range sp of S over KS stages (balanced;
+// S <= 16 and KS <= 4096, so 32-bit products suffice).  The unsplit call
+// takes no division: it sits on the path to each CTA's first weight copy.
 __device__ __forceinline__ void k_range(int sp, int S, int KS, int& kb, int& ke) {
-    kb = (int)(((long long)sp * KS) / S);
-    ke = (int)(((long long)(sp + 1) * KS) / S);
+    if (S == 1) {
+        kb = 0;
+        ke = KS;
+        return;
+    }
+    kb = (sp * KS) / S;
+    ke = ((sp + 1) * KS) / S;
 }
 
 __host__ __device__ constexpr int pow2_cols(int n) {
@@ -233,7 +250,7 @@ __device__ __forceinline__ unsigned long long epoch_arrive(unsigned long long* c
 // part; the last of the expert's 4 x (tiles) parts increments the expert's
 // signal.  Each lane fences its own stores first.
 template <int TT_MAX>
-__device__ __forceinline__ void signal_tile_part(const GemmParams& p, const TileCoord& tc, int lane) {
+__device__ __forceinline__ void signal_tile_part(const GemmArgs& p, const TileCoord& tc, int lane) {
     if (!p.signals) return;
     __threadfence();
     __syncwarp();
@@ -267,6 +284,12 @@ __device__ __forceinline__ TileCoord decode_tile(const int* cum, const int* gm, 
     c.m = gm[lo];
     const int local = tile - cum[lo];
     const int ntt = token_tiles<TT_MAX>(c.m);
+    if (ntt == 1) {   // the common decode case: no divisions
+        c.w = (c.m + 15) & ~15;
+        c.nt = local;
+        c.t0 = 0;
+        return c;
+    }
     c.w = token_width(c.m, ntt);
     c.nt = local / ntt;
     c.t0 = (local - c.nt * ntt) * c.w;
@@ -281,7 +304,7 @@ __device__ __forceinline__ TileCoord decode_tile(const int* cum, const int* gm, 
 // C is bf16 [G][M_max][N/2], output column = 64 * block + 16 * quarter + l.
 template <int TT_MAX, int STAGES, bool SWIGLU = false, int KSUB = 1>
 __global__ void __launch_bounds__(kThreads, 1)
-gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
+gemm_nt_masked_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
     using Cfg = KCfg<TT_MAX, STAGES, KSUB>;
     // ring stages per tile: K-tiles of 256 codes, KSUB per stage (the host
     // picks KSUB = 2 only where it divides K / 256)
@@ -404,7 +427,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         long long issued = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            const int tile = u / p.split;
+            const int tile = p.split == 1 ? u : u / p.split;
             int kb, ke;
             k_range(u - tile * p.split, p.split, KSS, kb, ke);
             const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
@@ -471,7 +494,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         uint32_t aph = 0;
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            const int tile = u / p.split;
+            const int tile = p.split == 1 ? u : u / p.split;
             int kb, ke;
             k_range(u - tile * p.split, p.split, KSS, kb, ke);
             const TileCoord tc = decode_tile<TT_MAX>(cum, gm, p.G, tile);
@@ -531,7 +554,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams p) {
         long long cnt = 0;      // stages walked
         bool ok = true;
         for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-            const int tile = u / p.split;
+            const int tile = p.split == 1 ? u : u / p.split;
             int kb, ke;
             k_range(u - tile * p.split, p.split, KSS, kb, ke);
             for (int ks = kb; ks < ke; ++ks) {

@@ -108,7 +108,7 @@ __device__ __forceinline__ TileCoord decode_pair_tile(const int* cum, const int*
 
 template <int TT_MAX, int STAGES>
 __global__ void __launch_bounds__(kPairThreads, 1)
-gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams p) {
+gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
     using Cfg = PairCfg<TT_MAX, STAGES>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);

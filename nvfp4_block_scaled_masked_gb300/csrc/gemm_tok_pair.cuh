@@ -111,7 +111,7 @@ __device__ __forceinline__ TileCoord decode_tok_tile(const int* cum, const int* 
 }
 
 __global__ void __launch_bounds__(kTokThreads, 1)
-gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams p,
+gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams<1> p,
                                const __grid_constant__ CUtensorMap tm_w) {
     using Cfg = TokPairCfg;
     constexpr int STAGES = Cfg::STAGES;
@@ -154,8 +154,8 @@ gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams p,
         tmem_relinquish_pair();
     }
     if (warp == 2 && lane == 0) {
-        prefetch_tmap(&p.tm_a[7]);
-        prefetch_tmap(&p.tm_asf[7]);
+        prefetch_tmap(&p.tm_a[0]);
+        prefetch_tmap(&p.tm_asf[0]);
         prefetch_tmap(&tm_w);
     }
     for (int g = threadIdx.x; g < p.G; g += kTokThreads) {
@@ -233,7 +233,7 @@ gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams p,
                                      wrow + 128 * ks);
                 } else if (role == 1) {
                     if (leader) mbar_arrive_expect_tx(bar_full + 8 * s, 2 * Cfg::T_TILE);
-                    tma_load_3d_pair(base + Cfg::OFF_T + s * Cfg::T_TILE, &p.tm_a[7], fl, ks * 128,
+                    tma_load_3d_pair(base + Cfg::OFF_T + s * Cfg::T_TILE, &p.tm_a[0], fl, ks * 128,
                                      trow, tc.g);
                 } else {
                     // the peer's empty barrier completed with this one (same
@@ -242,7 +242,7 @@ gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams p,
                     mbar_arrive_expect_tx(sb, Cfg::WSF_STAGE + Cfg::TSF_STAGE);
                     bulk_load_multicast(base + Cfg::OFF_WSF + s * Cfg::WSF_STAGE + rank * 2048,
                                         p.wsf + (wsf0 + 4 * (size_t)ks) * 512, 2048, sb, 0x3);
-                    tma_load_3d(base + Cfg::OFF_TSF + s * Cfg::TSF_STAGE, &p.tm_asf[7], sb, ks * 16,
+                    tma_load_3d(base + Cfg::OFF_TSF + s * Cfg::TSF_STAGE, &p.tm_asf[0], sb, ks * 16,
                                 trow, tc.g);
                 }
                 __syncwarp();

@@ -165,8 +165,44 @@ int check_gemm_shape(int G, int M_max, int N, int K) {
     return NVFP4GG_OK;
 }
 
+// Decode-sized experts (M_max <= 64): token tiles of at most 32, a deep ring
+// for the weight stream.  Larger experts: token tiles of up to 192, so that a
+// prefill expert's rows usually fit one tile and its weights stream once, and
+// each MMA instruction carries 128 x 192 x 64 (the issuing warp's per-stage
+// cost, not the tensor pipe, bounds compute-heavy tiles).
+constexpr int kNarrowTT = 32, kNarrowStages = 8;
+// decode tiles with K % 512 == 0: stages of two K-tiles (same bytes in flight)
+constexpr int kNarrowStages2 = 4;
+constexpr int kWideTT = 192, kWideStages = 4;
+// Larger experts with N a multiple of 256: CTA pairs (M = 256 per MMA),
+// token tiles of up to 192 split 96 + 96 rows, six ring stages.
+constexpr int kPairTT = 192, kPairStages = 6;
+// Automatic pair mode: CTA pairs for prefill calls up to this M_max (a few
+// token tiles per expert: the weight stream dominates and the pair's halved
+// token staging and deeper ring pay); compute-heavy experts stay single.
+constexpr int kPairAutoMaxRows = 256;
+// Token-major pairs: 128 token rows per CTA (one tensor-map box).
+constexpr int kTokTT = 128;
+
+// The host fills the maps of every width; a launch carries the NW widths
+// from map `first` on.
+using GemmParamsAll = GemmParams<kMaxWidths>;
+
+template <int NW>
+GemmParams<NW> launch_params(const GemmParamsAll& all, int first) {
+    static_assert(NW >= 1 && NW <= kMaxWidths, "map count");
+    GemmParams<NW> k;
+    std::memset(&k, 0, sizeof(k));
+    static_cast<GemmArgs&>(k) = static_cast<const GemmArgs&>(all);
+    for (int i = 0; i < NW; ++i) {
+        k.tm_a[i] = all.tm_a[first + i];
+        k.tm_asf[i] = all.tm_asf[first + i];
+    }
+    return k;
+}
+
 template <int TT, int ST, bool SWIGLU = false, int KSUB = 1>
-int launch_variant(DeviceState* d, int slot, const GemmParams& p, cudaStream_t stream) {
+int launch_variant(DeviceState* d, int slot, const GemmParamsAll& all, cudaStream_t stream) {
     using Cfg = KCfg<TT, ST, KSUB>;
     auto kern = gemm_nt_masked_kernel<TT, ST, SWIGLU, KSUB>;
     if (!d->attr_set[slot]) {
@@ -177,12 +213,12 @@ int launch_variant(DeviceState* d, int slot, const GemmParams& p, cudaStream_t s
     }
     int grid = d->sms;
     if (g_sm_cap > 0 && g_sm_cap < grid) grid = g_sm_cap;
-    kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(p);
+    kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(launch_params<TT / 16>(all, 0));
     return cuda_status(cudaGetLastError());
 }
 
 template <int TT, int ST>
-int launch_pair_variant(DeviceState* d, int slot, const GemmParams& p, cudaStream_t stream) {
+int launch_pair_variant(DeviceState* d, int slot, const GemmParamsAll& all, cudaStream_t stream) {
     using Cfg = PairCfg<TT, ST>;
     auto kern = gemm_nt_masked_pair_kernel<TT, ST>;
     if (!d->attr_set[slot]) {
@@ -206,7 +242,7 @@ int launch_pair_variant(DeviceState* d, int slot, const GemmParams& p, cudaStrea
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cuda_status(cudaLaunchKernelEx(&cfg, kern, p));
+    return cuda_status(cudaLaunchKernelEx(&cfg, kern, launch_params<TT / 16>(all, 0)));
 }
 
 // Tensor map of the prepared weight tiles as a 2-D u8 array of 128-byte rows
@@ -250,8 +286,10 @@ int weight_map(const void* B, uint64_t rows, CUtensorMap* out) {
     return NVFP4GG_OK;
 }
 
-int launch_tok_pair(DeviceState* d, int slot, const GemmParams& p, const CUtensorMap& tm_w,
+int launch_tok_pair(DeviceState* d, int slot, const GemmParamsAll& all, const CUtensorMap& tm_w,
                     cudaStream_t stream) {
+    // the kernel loads 128-row token boxes only (map index 7)
+    const GemmParams<1> p = launch_params<1>(all, kTokTT / 16 - 1);
     using Cfg = TokPairCfg;
     if (!d->attr_set[slot]) {
         if (cudaFuncSetAttribute(gemm_nt_masked_tok_pair_kernel,
@@ -278,24 +316,6 @@ int launch_tok_pair(DeviceState* d, int slot, const GemmParams& p, const CUtenso
     return cuda_status(cudaLaunchKernelEx(&cfg, gemm_nt_masked_tok_pair_kernel, p, tm_w));
 }
 
-// Decode-sized experts (M_max <= 64): token tiles of at most 32, a deep ring
-// for the weight stream.  Larger experts: token tiles of up to 192, so that a
-// prefill expert's rows usually fit one tile and its weights stream once, and
-// each MMA instruction carries 128 x 192 x 64 (the issuing warp's per-stage
-// cost, not the tensor pipe, bounds compute-heavy tiles).
-constexpr int kNarrowTT = 32, kNarrowStages = 8;
-// decode tiles with K % 512 == 0: stages of two K-tiles (same bytes in flight)
-constexpr int kNarrowStages2 = 4;
-constexpr int kWideTT = 192, kWideStages = 4;
-// Larger experts with N a multiple of 256: CTA pairs (M = 256 per MMA),
-// token tiles of up to 192 split 96 + 96 rows, six ring stages.
-constexpr int kPairTT = 192, kPairStages = 6;
-// Automatic pair mode: CTA pairs for prefill calls up to this M_max (a few
-// token tiles per expert: the weight stream dominates and the pair's halved
-// token staging and deeper ring pay); compute-heavy experts stay single.
-constexpr int kPairAutoMaxRows = 256;
-// Token-major pairs: 128 token rows per CTA (one tensor-map box).
-constexpr int kTokTT = 128;
 
 }  // namespace
 
@@ -486,7 +506,7 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
     const bool pair = pairable && !tok &&
                       (g_pair_mode == 1 || (g_pair_mode == 2 && M_max <= kPairAutoMaxRows));
     const int tt_max = narrow ? kNarrowTT : tok ? kTokTT : pair ? kPairTT : kWideTT;
-    GemmParams p;
+    GemmParamsAll p;
     std::memset(&p, 0, sizeof(p));
     // packed rows (M_total > 0): one group of M_total rows; else [G][M_max]
     if ((rc = M_total > 0 ? token_maps(A, A_sf, 1, M_total, K, tt_max, p.tm_a, p.tm_asf)
