@@ -111,6 +111,11 @@ int nvfp4_prepare_weights(const void* B, const void* B_sf, int G, int N, int K,
  * K % 256 == 0.  Asynchronous on `stream`; device-side failures (a wait past
  * its time limit, a bad masked_m) are recorded in the error word read by
  * nvfp4_gg_check_error.
+ * Decode calls (M_max <= 64) with K >= 6144 and at most SMs/4 weight tiles
+ * (G * ceil(M_max/32) * ceil(N/128), every expert counted full) split K as
+ * nvfp4_grouped_gemm_nt_masked_splitk with split_k = 0 does, reducing within
+ * thread-block clusters (no workspace); the result is deterministic and
+ * agrees with an unsplit call up to fp32 summation order.
  */
 int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
                                  const void* B_sf, const float* alpha, const int* masked_m,
@@ -119,13 +124,17 @@ int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B,
 /*
  * Split-K variant for decode-sized calls (M_max <= 64), the swap-AB path's
  * split-K: each weight tile's K range is cut into split_k contiguous ranges
- * computed by different CTAs, each leaving an fp32 partial in `workspace`;
- * the last range of a tile to finish sums the partials in range order (so
- * results are deterministic), applies alpha and stores bf16.  This keeps all
- * SMs streaming weights when there are fewer weight tiles than SMs (few
- * non-empty experts, small N).
+ * computed by different CTAs, and their fp32 partials are summed in range
+ * order (so results are deterministic), scaled by alpha and stored as bf16.
+ * This keeps more SMs streaming weights when there are fewer weight tiles
+ * than SMs (few non-empty experts, small N).  Up to 8 ranges run as one
+ * thread-block cluster per tile and reduce through distributed shared
+ * memory: the workspace is then not touched.  Larger splits, or an SM cap
+ * (nvfp4_gg_set_sm_count) below the split, reduce through the workspace:
+ * the last range of a tile to finish sums the partials.  Both reductions
+ * add in the same order, so they give the same bits.
  *   split_k    1..16, or 0 to choose from the tile count: floor(SMs / tiles),
- *              at most K/256 and 16
+ *              at most 6 and at most K/1024
  *   workspace  device scratch owned by the caller, 256-byte aligned, at least
  *              nvfp4_splitk_workspace_bytes(G, M_max, N, K, split_k) bytes
  *              (fp32 partials, then one 8-byte arrival counter per tile);
@@ -156,7 +165,9 @@ int nvfp4_grouped_gemm_nt_masked_splitk(const void* A, const void* A_sf, const v
  *   NVFP4GG_NOALLOC_MAX_SLOTS fp32 partial tiles of 32 x 128 (16 KiB each,
  *   4 MiB in all) plus one 8-byte arrival counter per slot (2 KiB).
  * A split call uses tiles x split slots, tiles = G * ceil(M_max/32) *
- * ceil(N/128) (every expert counted full).
+ * ceil(N/128) (every expert counted full); a split the cluster reduction
+ * takes (up to 8 ranges, see nvfp4_grouped_gemm_nt_masked_splitk) leaves the
+ * scratch untouched, but the slot limit below applies all the same.
  *   split_k  0: the automatic split of the workspace variant, lowered until
  *               tiles x split fits the scratch (1 = unsplit when even 2 does
  *               not fit);

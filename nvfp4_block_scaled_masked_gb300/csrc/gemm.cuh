@@ -74,6 +74,10 @@ struct GemmArgs {
     int split;
     float* ws_part;
     unsigned long long* ws_cnt;
+    // split-K within a thread-block cluster (csplit != 0, split <= 8): the
+    // grid is a multiple of split, cluster rank = K range, and the ranges of
+    // a tile reduce through distributed shared memory (no workspace)
+    int csplit;
     // per-expert completion signals (null: none): signals[g] is incremented
     // once per call after all of expert g's valid rows of C are stored;
     // sig_cnt[G] counts finished tile parts
@@ -175,9 +179,14 @@ struct KCfg {
     static constexpr int OFF_TSFP = OFF_WSF + STAGES * WSF_STAGE;
     static constexpr int OFF_EPI = OFF_TSFP + STAGES * TSF_STAGE;   // 4 warps x 16 tokens x 32 n bf16
     static constexpr int EPI_BYTES = 4 * 16 * 32 * 2;
-    static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
-    // full, sfull, empty, sfready per stage; acc full/empty per buffer; MMA drain
-    static constexpr int NUM_BARS = 4 * STAGES + 2 * ACC_BUFS + 1;
+    // cluster split-K (decode tiles): this K range's fp32 partial,
+    // [TT_MAX tokens][128 weight rows], read by the cluster's CTAs
+    static constexpr int PART_BYTES = TT_MAX <= 32 ? TT_MAX * 128 * 4 : 0;
+    static constexpr int OFF_PART = OFF_EPI + EPI_BYTES;
+    static constexpr int OFF_BAR = OFF_PART + PART_BYTES;
+    // full, sfull, empty, sfready per stage; acc full/empty per buffer; MMA
+    // drain; cluster split-K: partials ready, partials read
+    static constexpr int NUM_BARS = 4 * STAGES + 2 * ACC_BUFS + 3;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int OFF_TAB = (OFF_MISC + 16 + 15) & ~15;
     // cum[kGroupsMax + 1] (tile prefix), gm[kGroupsMax] (clamped masked_m),
@@ -209,6 +218,25 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_sleep(bar, parity, 1000u)) return true;
+        if ((it & 31u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                *abort_flag = 1;
+                record_error(err, NVFP4GG_ERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
+// wait_bounded for a barrier that CTAs of the cluster arrive on with
+// release: the completed phase is observed with a cluster-scope acquire.
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity,
+                                                     volatile int* abort_flag, int* err,
+                                                     unsigned long long timeout_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_cluster_sleep(bar, parity, 1000u)) return true;
         if ((it & 31u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > timeout_ns) {
@@ -316,6 +344,24 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
+    // Decode tiles: the first weight stages of this CTA's first unit are
+    // requested into L2 at once, before masked_m and the tile tables (a
+    // couple of microseconds) are known.  The unit is guessed as if every
+    // expert held one token tile (an unsplit decode call with no empty
+    // expert: then exact); a wrong guess only warms other weights.
+    if (TT_MAX <= 32 && warp == 0 && lane == 0) {
+        const int tile = blockIdx.x / p.split;
+        const int g = tile / p.NT;
+        if (g < p.G) {
+            int kb, ke;
+            k_range(blockIdx.x - tile * p.split, p.split, KSS, kb, ke);
+            const size_t wtile = ((size_t)g * p.NT + (tile - g * p.NT)) * (size_t)p.KS;
+            const uint8_t* src = p.wq + wtile * Cfg::W_TILE + (size_t)kb * Cfg::W_STAGE;
+            const int n = min(ke - kb, STAGES);
+            prefetch_l2_bulk(src, (uint32_t)n * Cfg::W_STAGE);
+        }
+    }
+
     const uint32_t bar_full = base + Cfg::OFF_BAR;               // operand tiles: 2 producers + bytes
     const uint32_t bar_sfull = bar_full + 8 * STAGES;            // scale rows: 2 producers + bytes
     const uint32_t bar_empty = bar_sfull + 8 * STAGES;           // MMA commit
@@ -323,6 +369,8 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
     const uint32_t bar_accf = bar_sfready + 8 * STAGES;          // MMA commit, last stage
     const uint32_t bar_acce = bar_accf + 8 * Cfg::ACC_BUFS;      // 4 epilogue warps
     const uint32_t bar_done = bar_acce + 8 * Cfg::ACC_BUFS;      // MMA thread's drain
+    const uint32_t bar_pready = bar_done + 8;                    // cluster split-K: partials stored
+    const uint32_t bar_pfree = bar_pready + 8;                   // cluster split-K: partials read
     uint32_t* misc = reinterpret_cast<uint32_t*>(sbase + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
     volatile int* epi_flag = reinterpret_cast<volatile int*>(misc + 2);   // split-K: last range
@@ -343,6 +391,9 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
             mbar_init(bar_acce + 8 * b, 4);
         }
         mbar_init(bar_done, 1);
+        // every CTA of the cluster arrives once per tile on each
+        mbar_init(bar_pready, p.csplit ? p.split : 1);
+        mbar_init(bar_pfree, p.csplit ? p.split : 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -370,6 +421,11 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
         if (p.signals && m == 0 && blockIdx.x == 0) atomicAdd(p.signals + g, 1);
     }
     __syncthreads();
+    // cluster split-K: every CTA's barriers are initialised before any CTA
+    // of the cluster arrives on them.  Every thread arrives here; only the
+    // epilogue warps, which arrive remotely, wait at once (their first
+    // remote arrive is microseconds away), the others at the kernel's end.
+    if (p.csplit) cluster_arrive();
     if (warp == 0) {
         const int per = (p.G + 31) / 32;
         const int lo = lane * per;
@@ -638,6 +694,8 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
         uint8_t* stage_buf = sbase + Cfg::OFF_EPI + ew * (16 * 32 * 2);
         int acc = 0;
         uint32_t aph = 0;
+        uint32_t ntile = 0;   // tiles reduced (cluster split-K barrier phases)
+        if (p.csplit) cluster_wait();
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
             const int tile = u / p.split;
             const int sp = u - tile * p.split;
@@ -730,6 +788,99 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_acce + 8 * acc);
                 signal_tile_part<TT_MAX>(p, tc, lane);
+            } else if (p.csplit) {
+                // split-K in a cluster: the CTA of cluster rank sp computed K
+                // range sp of this tile.  Each CTA leaves its fp32 partial in
+                // its own shared memory; CTA sp then sums token rows sp,
+                // sp + split, ... over all ranks in rank order (the order of
+                // the workspace reduction below) and stores them.  All CTAs
+                // of a cluster walk the same tiles, so the per-tile arrivals
+                // pair up.  As below, the 4 epilogue warps pass the same
+                // named barriers on every tile and leave together on a flag
+                // set under a barrier; after a timeout the peers' waits run
+                // out in turn, and the kernel's closing cluster barrier keeps
+                // every CTA's shared memory alive while peers may read it.
+                const uint32_t ph_t = ntile & 1u;
+                bool go = ok;
+                if (go && ntile > 0)   // peers have read this CTA's previous partial
+                    go = __all_sync(0xffffffffu, wait_bounded_cluster(bar_pfree, ph_t ^ 1u, abort_flag,
+                                                                      p.err, p.timeout_ns));
+                if (go) {
+                    // partial [token][128 weight rows]: lane = row, so each
+                    // token's 32 rows of this warp are one 128-byte row piece
+                    float* part = reinterpret_cast<float*>(sbase + Cfg::OFF_PART) + quad * 32 + lane;
+#pragma unroll 1
+                    for (int c = 0; c < TT_MAX / 16; ++c) {
+                        if (c * 16 >= tc.w) break;
+                        uint32_t r[16];
+                        tmem_ld_32x32b_x16(tbase + c * 16, r);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) part[(c * 16 + t) * 128] = __uint_as_float(r[t]);
+                    }
+                }
+                if (ok) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar_acce + 8 * acc);   // TMEM no longer needed
+                }
+                named_barrier_sync(1, 128);   // the 4 warps' partial rows are stored
+                if (ew == 0) {
+                    const int stop = __shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0);
+                    if (lane == 0) *epi_stop = stop;
+                    // lane q tells rank q; release at cluster scope publishes
+                    // the CTA's partial (ordered before it by the barrier).
+                    // One arrive per lane: a release arrive takes hundreds of
+                    // cycles, so they run side by side
+                    if (!stop && lane < p.split)
+                        mbar_arrive_remote_release(mapa_shared(bar_pready, (uint32_t)lane));
+                }
+                named_barrier_sync(1, 128);
+                if (*epi_stop) break;
+                const bool rd = __all_sync(0xffffffffu, wait_bounded_cluster(bar_pready, ph_t, abort_flag,
+                                                                             p.err, p.timeout_ns));
+                if (rd) {
+                    // token rows t = sp + split (ew + 4 i); lane: weight rows
+                    // 4 lane .. 4 lane + 3 (16-byte loads from every rank)
+                    const int ng = tc.nt * 128 + 4 * lane;
+                    const uint32_t part0 = base + Cfg::OFF_PART + 16u * lane;
+                    for (int t = sp + p.split * ew; t < tc.w; t += 4 * p.split) {
+                        const uint32_t a = part0 + (uint32_t)t * 512u;
+                        float4 v[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            if (q < p.split) v[q] = ld_shared_cluster_v4(mapa_shared(a, (uint32_t)q));
+                        float4 sum = v[0];
+#pragma unroll
+                        for (int q = 1; q < 8; ++q)
+                            if (q < p.split) {
+                                sum.x += v[q].x;
+                                sum.y += v[q].y;
+                                sum.z += v[q].z;
+                                sum.w += v[q].w;
+                            }
+                        const int tok = tc.t0 + t;
+                        const long long row = out_row(p, off, tc.g, tok);
+                        if (tok < t_end && ng < p.N && row >= 0) {
+                            uint2 o;
+                            o.x = pack_bf16x2(al * sum.x, al * sum.y);
+                            o.y = pack_bf16x2(al * sum.z, al * sum.w);
+                            *reinterpret_cast<uint2*>(p.C + row * p.N + ng) = o;
+                        }
+                    }
+                }
+                named_barrier_sync(1, 128);   // the 4 warps' reads of the partials are done
+                if (ew == 0) {
+                    const int stop = __shfl_sync(0xffffffffu, lane == 0 ? *abort_flag : 0, 0);
+                    if (lane == 0) *epi_stop = stop;
+                    // the reads completed (their values are stored): relaxed
+                    // arrives free the peers' partials, lane q for rank q
+                    if (!stop && lane < p.split)
+                        mbar_arrive_remote_relaxed(mapa_shared(bar_pfree, (uint32_t)lane));
+                }
+                named_barrier_sync(1, 128);
+                if (*epi_stop) break;
+                ++ntile;
             } else {
                 // split-K.  The 4 epilogue warps pass the same named-barrier
                 // sequence on every unit, even after a timeout (then they skip
@@ -816,6 +967,13 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::TMEM_COLS);
+    }
+    // cluster split-K: no CTA leaves while another may still read its
+    // partial or arrive on its barriers
+    if (p.csplit) {
+        if (warp < 5 || warp > 8) cluster_wait();   // the epilogue warps waited already
+        cluster_arrive();
+        cluster_wait();
     }
 }
 

@@ -33,6 +33,9 @@ struct DeviceState {
     int sms = 0;
     int* err = nullptr;          // device address of g_error_word
     bool attr_set[12] = {};      // per kernel variant: max dynamic smem set
+    // per kernel variant and cluster size 2..8: 0 not asked yet, 1 a cluster
+    // of that many CTAs fits the device, -1 it does not
+    int cluster_fits[12][9] = {};
 };
 
 std::mutex g_mu;
@@ -213,7 +216,35 @@ int launch_variant(DeviceState* d, int slot, const GemmParamsAll& all, cudaStrea
     }
     int grid = d->sms;
     if (g_sm_cap > 0 && g_sm_cap < grid) grid = g_sm_cap;
-    kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(launch_params<TT / 16>(all, 0));
+    GemmParams<TT / 16> k = launch_params<TT / 16>(all, 0);
+    if (k.csplit) {
+        // split-K in clusters of `split` CTAs: a grid of whole clusters
+        const int cs = k.split;
+        grid -= grid % cs;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = Cfg::SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int& fits = d->cluster_fits[slot][cs];
+        if (fits == 0) {
+            int n = 0;
+            fits = (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n > 0) ? 1 : -1;
+            cudaGetLastError();   // a refused query leaves no sticky error
+        }
+        if (fits > 0) return cuda_status(cudaLaunchKernelEx(&cfg, kern, k));
+        // no room for such clusters: the workspace reduction, else no split
+        k.csplit = 0;
+        if (!k.ws_part) k.split = 1;
+    }
+    kern<<<grid, kThreads, Cfg::SMEM_BYTES, stream>>>(k);
     return cuda_status(cudaGetLastError());
 }
 
@@ -469,12 +500,15 @@ size_t splitk_part_bytes(long long tiles, int split) {
     return (size_t)tiles * split * kNarrowTT * 128 * sizeof(float);
 }
 
+// Automatic split: as many ranges as whole sets of the tiles fit the SMs,
+// at most 6 (clusters of 8 measured slower than 6) and at least 4 K-tiles
+// per range.
 int auto_split(DeviceState* d, long long tiles, int K) {
-    const int ks = K / 256;
-    long long s = tiles > 0 ? d->sms / tiles : 1;
+    const int grid = (g_sm_cap > 0 && g_sm_cap < d->sms) ? g_sm_cap : d->sms;
+    long long s = tiles > 0 ? grid / tiles : 1;
+    if (s > 6) s = 6;
+    if (s > K / 1024) s = K / 1024;
     if (s < 1) s = 1;
-    if (s > ks) s = ks;
-    if (s > 16) s = 16;
     return (int)s;
 }
 
@@ -539,6 +573,12 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
         p.split = split;
         p.ws_part = ws_part;
         p.ws_cnt = ws_cnt;
+        // up to 8 ranges (the portable cluster size) reduce within a
+        // cluster through distributed shared memory; the workspace is then
+        // not touched
+        const int grid = (g_sm_cap > 0 && g_sm_cap < d->sms) ? g_sm_cap : d->sms;
+        p.csplit = (split <= 8 && !signals && grid >= split) ? 1 : 0;
+        if (!p.csplit && !ws_part) p.split = 1;   // no workspace to reduce through
     }
     if (signals) {
         unsigned long long* counts = nullptr;
@@ -574,8 +614,21 @@ extern "C" {
 int nvfp4_grouped_gemm_nt_masked(const void* A, const void* A_sf, const void* B, const void* B_sf,
                                  const float* alpha, const int* masked_m, void* C, int G, int M_max,
                                  int N, int K, void* stream) {
-    return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, 1, nullptr, nullptr,
-                       stream);
+    // Decode calls with few tiles (at most a quarter of the SMs: one or two
+    // experts) and a long K split K over thread-block clusters, so that each
+    // tile's weight stream runs on several SMs (measured faster for one
+    // expert at N = 2048 and 4096, K = 7168; slower at K = 4096); all other
+    // calls run unsplit.  The result is deterministic either way.
+    int split = 1;
+    DeviceState* d = nullptr;
+    if (M_max <= 64 && K >= 24 * 256 && check_gemm_shape(G, M_max, N, K) == NVFP4GG_OK &&
+        device_state(&d) == NVFP4GG_OK) {
+        const long long tiles = decode_tile_bound(G, M_max, N);
+        const int grid = (g_sm_cap > 0 && g_sm_cap < d->sms) ? g_sm_cap : d->sms;
+        if (tiles * 4 <= grid) split = auto_split(d, tiles, K);
+    }
+    return gemm_launch(A, A_sf, B, B_sf, alpha, masked_m, C, G, M_max, N, K, split, nullptr,
+                       nullptr, stream);
 }
 
 }  // extern "C"

@@ -298,6 +298,47 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr
                  : "memory");
 }
 
+// Arrive on an mbarrier of a CTA of the cluster (this one included) with
+// release at cluster scope: this thread's earlier writes, and those ordered
+// before them by a CTA barrier, are visible to the CTA that observes the
+// completed phase with a cluster-scope acquire.
+__device__ __forceinline__ void mbar_arrive_remote_release(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+// try_wait with a suspend-time hint and acquire at cluster scope.
+__device__ __forceinline__ bool mbar_try_wait_cluster_sleep(uint32_t bar, uint32_t parity,
+                                                            uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Hint: bring `bytes` (a multiple of 16) at global address src into L2.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// 16-byte load from the shared memory of a CTA of the cluster (an address
+// from mapa_shared).
+__device__ __forceinline__ float4 ld_shared_cluster_v4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 // try_wait with acquire at cluster scope (for barriers that CTAs of the
 // cluster arrive on remotely).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
@@ -310,6 +351,16 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
         : "r"(bar), "r"(parity)
         : "memory");
     return ok != 0;
+}
+
+// The two halves of a cluster barrier, for threads that reach them at
+// different points (not .aligned): each thread arrives, and later waits for
+// every thread of the cluster to have arrived, once per phase.
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
 }
 
 __device__ __forceinline__ void cluster_sync_all() {

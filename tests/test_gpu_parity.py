@@ -201,6 +201,42 @@ def test_splitk_decode(lib, G, M_max, N, K, masked, split):
     check_full(d, run_gpu_splitk(d, split))
 
 
+# Splits of up to 8 ranges reduce inside a thread-block cluster (distributed
+# shared memory), larger ones through the workspace.  Several tiles per
+# cluster exercise the per-tile hand-offs; an SM cap below the split falls
+# back to the workspace; ragged N and token tails are stored by the cluster
+# epilogue.
+@pytest.mark.parametrize("G,M_max,N,K,masked,split,cap", [
+    (4, 64, 2048, 4096, [64, 33, 0, 50], 8, 0),   # 96 tiles on 19 clusters of 8
+    (2, 40, 1040, 7168, [40, 7], 5, 0),           # clusters of 5 (grid 150), N tail
+    (1, 32, 4096, 7168, [32], 12, 0),             # more than 8 ranges: workspace
+    (3, 48, 512, 2048, [48, 1, 17], 4, 6),        # SM cap 6: one cluster of 4
+    (2, 16, 256, 1024, [16, 9], 4, 3),            # SM cap 3 < split: workspace
+])
+def test_splitk_cluster_and_workspace(lib, G, M_max, N, K, masked, split, cap):
+    d = W.generate(W.custom(G, M_max, N, K, masked_m=masked), seed=7 * G + N + K)
+    lib.nvfp4_gg_set_sm_count(cap)
+    try:
+        check_full(d, run_gpu_splitk(d, split))
+    finally:
+        lib.nvfp4_gg_set_sm_count(0)
+
+
+def test_splitk_cluster_equals_workspace_bits(lib):
+    """Four ranges reduce in a cluster when 4 SMs or more are allowed, through
+    the workspace under an SM cap of 3; both add the same partials in range
+    order, so the bits agree."""
+    d = W.generate(W.custom(2, 40, 1296, 7168, masked_m=[40, 19]), seed=4242)
+    cluster = run_gpu_splitk(d, 4)
+    lib.nvfp4_gg_set_sm_count(3)
+    try:
+        workspace = run_gpu_splitk(d, 4)
+    finally:
+        lib.nvfp4_gg_set_sm_count(0)
+    np.testing.assert_array_equal(cluster, workspace)
+    check_full(d, cluster)
+
+
 def test_c2_decode_full(lib):
     d = W.generate(W.CONFIGS["c2"])
     check_full(d, run_gpu(d))
