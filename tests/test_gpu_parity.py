@@ -222,6 +222,36 @@ def test_splitk_cluster_and_workspace(lib, G, M_max, N, K, masked, split, cap):
         lib.nvfp4_gg_set_sm_count(0)
 
 
+@pytest.mark.parametrize("G,N,masked", [
+    (1, 2048, [7]),          # 16 tiles: 6 ranges per tile
+    (1, 4096, [32]),         # 32 tiles: 4 ranges
+    (2, 1040, [5, 0]),       # 18 tiles (N tail, one expert empty)
+])
+def test_plain_entry_splits_few_tile_decode_calls(lib, G, N, masked):
+    """The plain entry point splits decode calls with at most SMs/4 tiles
+    and K >= 6144 over thread-block clusters: within the tolerance, rows
+    past masked_m untouched, two calls bit-identical; under SM caps (10: 2
+    ranges of a single... or fewer; 3: too few SMs to split) the results stay
+    within the tolerance."""
+    from nvfp4_block_scaled_masked_gb300.device import Problem
+    d = W.generate(W.custom(G, 32, N, 7168, masked_m=masked), seed=G * 7 + N)
+    prob = Problem(d)
+    outs = []
+    for cap in (0, 0, 70, 3):
+        lib.nvfp4_gg_set_sm_count(cap)
+        try:
+            prob.reset_C()
+            prob.run()
+            rc = lib.nvfp4_gg_check_error()
+            assert rc == 0, lib.status_string(rc)
+            outs.append(prob.C_bits())
+        finally:
+            lib.nvfp4_gg_set_sm_count(0)
+    np.testing.assert_array_equal(outs[0], outs[1])
+    for C in outs:
+        check_full(d, C)
+
+
 def test_splitk_cluster_equals_workspace_bits(lib):
     """Four ranges reduce in a cluster when 4 SMs or more are allowed, through
     the workspace under an SM cap of 3; both add the same partials in range
