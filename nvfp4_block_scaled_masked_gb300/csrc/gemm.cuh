@@ -14,13 +14,16 @@
 // operation, tcgen05 copy/MMA/commit) occupies its issuing thread for tens of
 // cycles (hundreds under load), so the per-stage work is spread over several
 // issuing threads:
-//   warp 0      weight producer (one lane): bulk copies of the 16 KB weight
-//               tile and its 2 KB scale atoms into the shared ring.
+//   warp 0      weight producer (one lane): bulk copies of the stage's
+//               weight tiles (16 KB per 256-code K-tile, KSUB K-tiles per
+//               stage, contiguous in the prepared layout) and their scale
+//               atoms (2 KB per K-tile) into the shared ring.
 //   warp 1      TMEM owner; MMA warp: walks the stages as a warp, one
-//               elected lane issues 4 x tcgen05.mma (K = 64 each) per stage
+//               elected lane issues 4 x tcgen05.mma (K = 64 each) per K-tile
 //               and the commit of the stage back to the producers.
-//   warp 2      token producer (one lane): one tiled TMA for the w token rows
-//               and one for their scale rows (a tensor map per width w).
+//   warp 2      token producer (one lane): per K-tile one tiled TMA for the
+//               w token rows and one for their scale rows (a tensor map per
+//               width w).
 //   warps 3, 4, 9, 10  scale warps, one per TMEM lane quarter: every stage,
 //               each lane loads its scale words from shared memory and the
 //               warp writes them into its quarter with tcgen05.st (no
