@@ -38,9 +38,10 @@
  *     nvfp4_gg_set_sm_count is process-wide.
  *   - Per device the library looks up, on its first call there, the device
  *     addresses of its static __device__ arrays (error word, signal
- *     counters, split-K scratch) and keeps them for the life of the process.
- *     A cudaDeviceReset invalidates them: do not call into the library on a
- *     device after resetting it in the same process.
+ *     counters, split-K scratch), sets its kernels' shared-memory limits and
+ *     caches tensor maps; it keeps all of it until nvfp4_gg_shutdown.  A
+ *     cudaDeviceReset invalidates it: call nvfp4_gg_shutdown after resetting
+ *     a device before calling into the library there again.
  */
 #ifndef NVFP4GG_H
 #define NVFP4GG_H
@@ -406,6 +407,17 @@ int nvfp4_gg_set_sm_count(int sm_count);
  * NVFP4GG_ERR_SHAPE unless 0, 1, 2 or 3.
  */
 int nvfp4_gg_set_pair_mode(int mode);
+
+/*
+ * Drops every host-side cache of the library: per-device state (SM count,
+ * error-word and scratch addresses, kernel attributes, cluster fits) and
+ * the tensor-map caches.  The library holds no device allocation, so
+ * nothing is freed on the device; the next call on a device sets it up
+ * again.  Call it after a cudaDeviceReset, or when done with the library.
+ * It must not run while another thread is inside a library call.  Returns
+ * NVFP4GG_OK.
+ */
+int nvfp4_gg_shutdown(void);
 
 /*
  * Synchronises `stream`, then reads and clears the current device's error

@@ -45,6 +45,7 @@ EXPORTS = (
     "nvfp4_grouped_gemm_nt_masked_host",
     "nvfp4_gg_set_sm_count",
     "nvfp4_gg_set_pair_mode",
+    "nvfp4_gg_shutdown",
     "nvfp4_gg_check_error",
     "nvfp4_gg_selftest_watchdog",
     "nvfp4_gg_mma_peak_probe",
@@ -110,6 +111,8 @@ def load():
     lib.nvfp4_gg_set_sm_count.restype = i
     lib.nvfp4_gg_set_pair_mode.argtypes = [i]
     lib.nvfp4_gg_set_pair_mode.restype = i
+    lib.nvfp4_gg_shutdown.argtypes = []
+    lib.nvfp4_gg_shutdown.restype = i
     lib.nvfp4_gg_check_error.argtypes = [vp]
     lib.nvfp4_gg_check_error.restype = i
     lib.nvfp4_gg_selftest_watchdog.argtypes = [ctypes.c_longlong, vp]
@@ -289,6 +292,12 @@ def nvfp4_gg_set_pair_mode(mode):
     2: automatic (the library's default)."""
     m = (1 if mode else 0) if isinstance(mode, bool) else int(mode)
     _check(load().nvfp4_gg_set_pair_mode(m), "nvfp4_gg_set_pair_mode")
+
+
+def nvfp4_gg_shutdown():
+    """Drops the library's host-side caches (after a device reset, or when
+    done); the next call sets the device up again."""
+    _check(load().nvfp4_gg_shutdown(), "nvfp4_gg_shutdown")
 
 
 def nvfp4_gg_check_error(stream=None) -> int:

@@ -36,6 +36,7 @@ struct DeviceState {
     // per kernel variant and cluster size 2..8: 0 not asked yet, 1 a cluster
     // of that many CTAs fits the device, -1 it does not
     int cluster_fits[12][9] = {};
+    bool gemv_attr[9] = {};      // per GEMV token count: max dynamic smem set
 };
 
 std::mutex g_mu;
@@ -641,14 +642,11 @@ int launch_gemv(DeviceState* d, const void* x, const void* B, const void* B_sf, 
     constexpr int R = M <= 4 ? 2 : 1;   // weight rows per warp (register budget, grid balance)
     auto kern = gemv_w4a16_kernel<M, R>;
     const int smem = (int)gemv_smem_bytes(M, K);
-    static bool attr_done[kMaxDevices] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4GG_ERR_CUDA;
-    if (!attr_done[dev]) {
+    if (!d->gemv_attr[M]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kGemvMaxSmem) != cudaSuccess)
             return NVFP4GG_ERR_CUDA;
-        attr_done[dev] = true;
+        d->gemv_attr[M] = true;
     }
     // as many CTAs per SM as registers and the staged tokens allow, groups of
     // R rows grid-strided over all warps
@@ -1036,3 +1034,22 @@ extern "C" int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(
                        reinterpret_cast<float*>(scratch),
                        reinterpret_cast<unsigned long long*>(scratch + kNoAllocPartBytes), stream);
 }
+
+// ---------------------------------------------------------------------------
+// Dropping the host-side caches (every other file-scope cache is above).
+
+extern "C" {
+
+int nvfp4_gg_shutdown(void) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    for (int i = 0; i < kMaxDevices; ++i) {
+        g_dev[i] = DeviceState{};
+        g_signal_addr[i] = nullptr;
+        g_noalloc_addr[i] = nullptr;
+    }
+    for (int i = 0; i < kMapCache; ++i) g_maps[i].A = nullptr;
+    for (int i = 0; i < kWeightMapCache; ++i) g_wmaps[i].B = nullptr;
+    return NVFP4GG_OK;
+}
+
+}  // extern "C"

@@ -157,6 +157,13 @@ def test_sm_cap_and_watchdog_argument_checks(lib):
     assert lib.nvfp4_gg_selftest_watchdog(10 ** 11, None) == binding.ERR_SHAPE
 
 
+def test_shutdown_is_host_only_and_repeatable(lib):
+    """nvfp4_gg_shutdown touches no device: it works here, with no GPU, and
+    twice in a row; the settings (SM cap, pair mode) are not caches and stay."""
+    assert lib.nvfp4_gg_shutdown() == binding.OK
+    assert lib.nvfp4_gg_shutdown() == binding.OK
+
+
 def test_library_targets_sm103a_only():
     assert build.ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -359,6 +359,29 @@ def test_sm_count_cap_gives_identical_results(lib, G, M_max, N, K, masked):
     check_full(d, ref)
 
 
+def test_calls_after_shutdown_set_the_device_up_again(lib):
+    """After nvfp4_gg_shutdown the next calls rebuild the device state, the
+    kernels' shared-memory limits and the tensor maps: a decode call split
+    in clusters and a prefill call on CTA pairs give the same bits as before
+    it."""
+    from nvfp4_block_scaled_masked_gb300.device import Problem
+    ds = [W.generate(W.custom(1, 8, 2048, 7168, masked_m=[5]), seed=3),      # cluster split
+          W.generate(W.custom(3, 200, 512, 768, masked_m=[200, 5, 130]), seed=4)]   # pairs
+    probs = [Problem(d) for d in ds]
+    before = []
+    for prob in probs:
+        prob.run()
+        assert lib.nvfp4_gg_check_error() == 0
+        before.append(prob.C_bits())
+    lib.nvfp4_gg_shutdown()
+    for d, prob, ref in zip(ds, probs, before):
+        prob.reset_C()
+        prob.run()
+        assert lib.nvfp4_gg_check_error() == 0
+        np.testing.assert_array_equal(prob.C_bits(), ref)
+        check_full(d, ref)
+
+
 def test_mma_peak_probe_runs_clean(lib):
     lib.nvfp4_gg_mma_peak_probe(64, 256)
     lib.nvfp4_gg_mma_peak_probe(64, 16, 3)
