@@ -428,41 +428,45 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
     // of the cluster arrives on them.  Every thread arrives here; only the
     // epilogue warps, which arrive remotely, wait at once (their first
     // remote arrive is microseconds away), the others at the kernel's end.
-    if (p.csplit) cluster_arrive();
+    // Thread 0 published the initialisation with fence.mbarrier_init, so a
+    // relaxed arrive suffices.
+    if (p.csplit) cluster_arrive_relaxed();
     if (warp == 0) {
-        const int per = (p.G + 31) / 32;
+        // Both prefixes in one pass: tile counts (the tile list) and valid
+        // rows (row offsets of the packed-rows layout).  It sits on the path
+        // to every CTA's first weight copy: the two shuffle chains run side
+        // by side and each parameter is read once.
+        const int G = p.G, NT = p.NT;
+        const int per = (G + 31) / 32;
         const int lo = lane * per;
-        const int hi = min(p.G, lo + per);
-        int sum = 0;
-        for (int g = lo; g < hi; ++g) sum += token_tiles<TT_MAX>(gm[g]) * p.NT;
-        int incl = sum;
+        const int hi = min(G, lo + per);
+        int sum = 0, rs = 0;
+        for (int g = lo; g < hi; ++g) {
+            const int m = gm[g];
+            sum += token_tiles<TT_MAX>(m) * NT;
+            rs += m;
+        }
+        int incl = sum, rincl = rs;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
+            const int w = __shfl_up_sync(0xffffffffu, rincl, o);
+            if (lane >= o) {
+                incl += v;
+                rincl += w;
+            }
         }
-        int run = incl - sum;
+        int run = incl - sum, rrun = rincl - rs;
         for (int g = lo; g < hi; ++g) {
+            const int m = gm[g];
             cum[g] = run;
-            run += token_tiles<TT_MAX>(gm[g]) * p.NT;
-        }
-        if (lane == 31) cum[p.G] = incl;
-        // row offsets of the packed-rows layout
-        int rs = 0;
-        for (int g = lo; g < hi; ++g) rs += gm[g];
-        int rincl = rs;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, rincl, o);
-            if (lane >= o) rincl += v;
-        }
-        int rrun = rincl - rs;
-        for (int g = lo; g < hi; ++g) {
             off[g] = rrun;
-            rrun += gm[g];
+            run += token_tiles<TT_MAX>(m) * NT;
+            rrun += m;
         }
         if (lane == 31) {
-            off[p.G] = rincl;
+            cum[G] = incl;
+            off[G] = rincl;
             if (p.contiguous && rincl > p.M_total) record_error(p.err, NVFP4GG_ERR_MASK);
         }
     }
