@@ -328,7 +328,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="c4", choices=sorted(W.CONFIGS) + sorted(W.EXTRA))
-    ap.add_argument("--per-config-steps", type=int, default=30,
+    ap.add_argument("--per-config-steps", type=int, default=100,
                     help="timed steps per workload in the per_config block (0: no per_config)")
     ap.add_argument("--splitk", type=int, default=-1,
                     help="time nvfp4_grouped_gemm_nt_masked_splitk with this split (0 = automatic)")
