@@ -327,6 +327,67 @@ __device__ __forceinline__ TileCoord decode_tile(const int* cum, const int* gm, 
     return c;
 }
 
+// The SwiGLU epilogue of one tile on the swap-AB kernels (TMEM lane = prepared
+// weight row, column = token): 16-token chunks; lane l < 16 combines its
+// h_gate = alpha * acc with lane l + 16's h_up into silu(h_gate) * h_up for
+// output column 64 * block + 16 * quad + l, where `block` is the tile's
+// 128-row weight block; the [16 tokens][16 columns] bf16 chunk is staged in
+// `stage_buf` (512 bytes) and stored, and with qa set lane t < 16 also
+// encodes token t's 16 columns as one NVFP4 block of GEMM2's K.
+template <int TT_MAX>
+__device__ __forceinline__ void swiglu_tile_store(const GemmArgs& p, const int* off,
+                                                  const TileCoord& tc, uint32_t tbase, int block,
+                                                  int quad, int lane, float al,
+                                                  uint8_t* stage_buf) {
+    const int NO = p.N >> 1;
+    const int oc0 = block * 64 + quad * 16;
+    const int t_end = min(tc.t0 + tc.w, tc.m);
+    const bool quant = p.qa != nullptr;
+    const float qs = quant ? __ldg(p.qscale + tc.g) : 0.f;
+    __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stage_buf);
+#pragma unroll 1
+    for (int c = 0; c < TT_MAX / 16; ++c) {
+        if (c * 16 >= tc.w) break;
+        uint32_t r[16];
+        tmem_ld_32x32b_x16(tbase + c * 16, r);
+        tmem_wait_ld();
+        // all 32 lanes compute: lane l < 16 token 2j of column l (its own
+        // gate, lane l + 16's up), lane l + 16 token 2j + 1 of the same
+        // column (lane l's gate, its own up)
+        const bool lo = lane < 16;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float h0 = al * __uint_as_float(r[2 * j]);
+            const float h1 = al * __uint_as_float(r[2 * j + 1]);
+            const float p0 = __shfl_xor_sync(0xffffffffu, h0, 16);
+            const float p1 = __shfl_xor_sync(0xffffffffu, h1, 16);
+            const float gate = lo ? h0 : p1;
+            const float up = lo ? p0 : h1;
+            const float y = __fdividef(gate * up, 1.0f + __expf(-gate));   // silu(gate) * up
+            sb[(2 * j + (lo ? 0 : 1)) * 16 + (lane & 15)] = __float2bfloat16_rn(y);
+        }
+        __syncwarp();
+        const int t = lane >> 1, hh = lane & 1;
+        const int tok = tc.t0 + c * 16 + t;
+        const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + t * 32 + hh * 16);
+        const long long row = out_row(p, off, tc.g, tok);
+        if (p.C && tok < t_end && oc0 < NO && row >= 0)
+            *reinterpret_cast<uint4*>(p.C + row * NO + oc0 + 8 * hh) = v;
+        if (quant && lane < 16) {
+            const int qtok = tc.t0 + c * 16 + lane;
+            const long long qrow = out_row(p, off, tc.g, qtok);
+            if (qtok < t_end && oc0 < NO && qrow >= 0) {
+                const uint4* src = reinterpret_cast<const uint4*>(stage_buf + lane * 32);
+                uint2 qc;
+                const uint32_t qsb = nvfp4_quant_block16(src[0], src[1], qs, qc);
+                *reinterpret_cast<uint2*>(p.qa + qrow * (NO >> 1) + (oc0 >> 1)) = qc;
+                p.qsf[qrow * (NO >> 4) + (oc0 >> 4)] = static_cast<uint8_t>(qsb);
+            }
+        }
+        __syncwarp();
+    }
+}
+
 // SWIGLU: the fused GEMM1 epilogue.  The weights are prepared with gate and
 // up rows interleaved (nvfp4_prepare_weights_swiglu): in each 32-row lane
 // quarter of a 128-row block, rows 0..15 are gate rows and rows 16..31 the
@@ -721,49 +782,7 @@ gemm_nt_masked_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
             const bool n_ok = n0 + 8 * tq < p.N;
             __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stage_buf);
             if (SWIGLU) {
-                // output columns oc0 .. oc0 + 15 of this warp; a stage of
-                // [16 tokens][16 columns] bf16, stored by 32 lanes x 16 bytes
-                const int NO = p.N >> 1;
-                const int oc0 = tc.nt * 64 + quad * 16;
-                // NVFP4 output: this warp's 16 columns are one 16-element
-                // block of GEMM2's K, i.e. token t's block is row t of the
-                // staged bf16 tile; lane t < 16 encodes it after the tile
-                // is staged
-                const bool quant = p.qa != nullptr;
-                const float qs = quant ? __ldg(p.qscale + tc.g) : 0.f;
-#pragma unroll 1
-                for (int c = 0; c < TT_MAX / 16; ++c) {
-                    if (c * 16 >= tc.w) break;
-                    uint32_t r[16];
-                    tmem_ld_32x32b_x16(tbase + c * 16, r);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        const float h = al * __uint_as_float(r[t]);
-                        const float up = __shfl_xor_sync(0xffffffffu, h, 16);
-                        const float y = h / (1.0f + __expf(-h)) * up;   // lanes < 16: silu(gate) * up
-                        if (lane < 16) sb[t * 16 + lane] = __float2bfloat16_rn(y);
-                    }
-                    __syncwarp();
-                    const int t = lane >> 1, hh = lane & 1;
-                    const int tok = tc.t0 + c * 16 + t;
-                    const uint4 v = *reinterpret_cast<const uint4*>(stage_buf + t * 32 + hh * 16);
-                    const long long row = out_row(p, off, tc.g, tok);
-                    if (p.C && tok < t_end && oc0 < NO && row >= 0)
-                        *reinterpret_cast<uint4*>(p.C + row * NO + oc0 + 8 * hh) = v;
-                    if (quant && lane < 16) {
-                        const int qtok = tc.t0 + c * 16 + lane;
-                        const long long qrow = out_row(p, off, tc.g, qtok);
-                        if (qtok < t_end && oc0 < NO && qrow >= 0) {
-                            const uint4* src = reinterpret_cast<const uint4*>(stage_buf + lane * 32);
-                            uint2 qc;
-                            const uint32_t qsb = nvfp4_quant_block16(src[0], src[1], qs, qc);
-                            *reinterpret_cast<uint2*>(p.qa + qrow * (NO >> 1) + (oc0 >> 1)) = qc;
-                            p.qsf[qrow * (NO >> 4) + (oc0 >> 4)] = static_cast<uint8_t>(qsb);
-                        }
-                    }
-                    __syncwarp();
-                }
+                swiglu_tile_store<TT_MAX>(p, off, tc, tbase, tc.nt, quad, lane, al, stage_buf);
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(bar_acce + 8 * acc);

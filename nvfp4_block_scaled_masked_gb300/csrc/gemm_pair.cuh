@@ -106,7 +106,10 @@ __device__ __forceinline__ TileCoord decode_pair_tile(const int* cum, const int*
     return c;
 }
 
-template <int TT_MAX, int STAGES>
+// SWIGLU: the fused GEMM1 epilogue of the single-CTA kernels (weights
+// prepared with gate and up rows interleaved per lane quarter), on this
+// CTA's weight block 2 nt + rank.
+template <int TT_MAX, int STAGES, bool SWIGLU = false>
 __global__ void __launch_bounds__(kPairThreads, 1)
 gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
     using Cfg = PairCfg<TT_MAX, STAGES>;
@@ -406,8 +409,11 @@ gemm_nt_masked_pair_kernel(const __grid_constant__ GemmParams<TT_MAX / 16> p) {
             const uint32_t tbase = tmem + acc * TT_MAX + ((uint32_t)(quad * 32) << 16);
             const int tr = lane >> 2, tq = lane & 3;
             const bool n_ok = n0 + 8 * tq < p.N;
+            if (SWIGLU)
+                swiglu_tile_store<TT_MAX>(p, off, tc, tbase, 2 * tc.nt + (int)rank, quad, lane, al,
+                                          stage_buf);
 #pragma unroll 1
-            for (int c = 0; c < TT_MAX / 16; ++c) {
+            for (int c = 0; c < (SWIGLU ? 0 : TT_MAX / 16); ++c) {
                 if (c * 16 >= tc.w) break;
                 uint32_t rr[16];
                 tmem_ld_32x32b_x16(tbase + c * 16, rr);

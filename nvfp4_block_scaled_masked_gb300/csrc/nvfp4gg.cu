@@ -249,10 +249,10 @@ int launch_variant(DeviceState* d, int slot, const GemmParamsAll& all, cudaStrea
     return cuda_status(cudaGetLastError());
 }
 
-template <int TT, int ST>
+template <int TT, int ST, bool SWIGLU = false>
 int launch_pair_variant(DeviceState* d, int slot, const GemmParamsAll& all, cudaStream_t stream) {
     using Cfg = PairCfg<TT, ST>;
-    auto kern = gemm_nt_masked_pair_kernel<TT, ST>;
+    auto kern = gemm_nt_masked_pair_kernel<TT, ST, SWIGLU>;
     if (!d->attr_set[slot]) {
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  Cfg::SMEM_BYTES) != cudaSuccess)
@@ -535,12 +535,16 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
     // (same token tile bound, same tensor maps) runs the call instead
     const bool pair_fits = g_sm_cap == 0 || g_sm_cap >= 2;
     const bool pairable = !narrow && !swiglu && !signals && N % 256 == 0 && pair_fits;
+    // the SwiGLU epilogue runs on CTA pairs too (not on the token-major
+    // ones), in pair modes 1 and 2
+    const bool swiglu_pair = !narrow && swiglu && !signals && N % 256 == 0 && pair_fits &&
+                             (g_pair_mode == 1 || g_pair_mode == 2);
     // token-major pairs (256 x 256 MMA tiles) for compute-heavy experts
     const bool tok = pairable && M_total == 0 && M_max >= 128 && G <= TokPairCfg::MAX_GROUPS &&
                      (g_pair_mode == 3 || (g_pair_mode == 2 && M_max > kPairAutoMaxRows));
     const bool pair = pairable && !tok &&
                       (g_pair_mode == 1 || (g_pair_mode == 2 && M_max <= kPairAutoMaxRows));
-    const int tt_max = narrow ? kNarrowTT : tok ? kTokTT : pair ? kPairTT : kWideTT;
+    const int tt_max = narrow ? kNarrowTT : tok ? kTokTT : (pair || swiglu_pair) ? kPairTT : kWideTT;
     GemmParamsAll p;
     std::memset(&p, 0, sizeof(p));
     // packed rows (M_total > 0): one group of M_total rows; else [G][M_max]
@@ -593,6 +597,7 @@ int gemm_launch(const void* A, const void* A_sf, const void* B, const void* B_sf
     const bool ksub2 = narrow && p.KS % 2 == 0 && p.split * 2 <= p.KS;
     if (swiglu) {
         if (ksub2) return launch_variant<kNarrowTT, kNarrowStages2, true, 2>(d, 7, p, st);
+        if (swiglu_pair) return launch_pair_variant<kPairTT, kPairStages, true>(d, 8, p, st);
         return narrow ? launch_variant<kNarrowTT, kNarrowStages, true>(d, 3, p, st)
                       : launch_variant<kWideTT, kWideStages, true>(d, 4, p, st);
     }

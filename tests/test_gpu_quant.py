@@ -113,11 +113,21 @@ def _pow2_prescale(y_max):
     return np.float32(2.0) ** np.floor(np.log2(2688.0 / max(y_max, 1e-30))).astype(np.float32)
 
 
-@pytest.mark.parametrize("case", ["narrow", "wide", "decode_gemm1"])
+@pytest.mark.parametrize("case", ["narrow", "wide", "wide_pair", "decode_gemm1"])
 def test_swiglu_quant_and_chain(lib, case):
+    # "wide": the single-CTA prefill kernel (pair mode 0); "wide_pair": the
+    # same shape on CTA pairs (automatic mode, N % 256 == 0)
+    lib.nvfp4_gg_set_pair_mode(0 if case == "wide" else lib.PAIR_AUTO)
+    try:
+        _swiglu_quant_and_chain(lib, case)
+    finally:
+        lib.nvfp4_gg_set_pair_mode(lib.PAIR_AUTO)
+
+
+def _swiglu_quant_and_chain(lib, case):
     if case == "narrow":
         d = W.generate(W.custom(3, 40, 512, 512, masked_m=[40, 0, 17]), seed=91)
-    elif case == "wide":
+    elif case in ("wide", "wide_pair"):
         d = W.generate(W.custom(2, 200, 512, 1024, masked_m=[200, 77]), seed=92)
     else:
         d = W.generate(W.CONFIGS["c2"])

@@ -73,14 +73,22 @@ def check(d, C_gpu):
     assert same > 0.9, f"only {same:.3f} bit-identical to the correctly rounded oracle"
 
 
+@pytest.mark.parametrize("pair", [0, 2])         # single-CTA kernels; automatic (CTA pairs where N % 256 == 0)
 @pytest.mark.parametrize("G,M_max,N,K,masked", [
     (3, 40, 256, 512, [40, 0, 17]),              # decode kernel, two token tiles, an empty expert
     (2, 200, 384, 1024, [200, 77]),              # prefill kernel, ragged token tiles
+    (2, 200, 512, 1024, [200, 77]),              # prefill, N % 256 == 0: CTA pairs in mode 2
+    (3, 300, 768, 2048, [300, 0, 129]),          # several token tiles per expert, an empty expert
     (1, 1, 128, 256, [1]),                       # minimum sizes
 ])
-def test_swiglu_shapes(lib, G, M_max, N, K, masked):
+def test_swiglu_shapes(lib, G, M_max, N, K, masked, pair):
     d = W.generate(W.custom(G, M_max, N, K, masked_m=masked), seed=G * 7 + N + K)
-    check(d, run_swiglu(lib, d))
+    lib.nvfp4_gg_set_pair_mode(pair)
+    try:
+        C = run_swiglu(lib, d)
+    finally:
+        lib.nvfp4_gg_set_pair_mode(lib.PAIR_AUTO)
+    check(d, C)
 
 
 def test_swiglu_decode_gemm1_full(lib):
