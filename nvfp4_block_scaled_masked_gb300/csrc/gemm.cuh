@@ -373,15 +373,14 @@ __device__ __forceinline__ void swiglu_tile_store(const GemmArgs& p, const int* 
         const long long row = out_row(p, off, tc.g, tok);
         if (p.C && tok < t_end && oc0 < NO && row >= 0)
             *reinterpret_cast<uint4*>(p.C + row * NO + oc0 + 8 * hh) = v;
-        if (quant && lane < 16) {
-            const int qtok = tc.t0 + c * 16 + lane;
-            const long long qrow = out_row(p, off, tc.g, qtok);
-            if (qtok < t_end && oc0 < NO && qrow >= 0) {
-                const uint4* src = reinterpret_cast<const uint4*>(stage_buf + lane * 32);
-                uint2 qc;
-                const uint32_t qsb = nvfp4_quant_block16(src[0], src[1], qs, qc);
-                *reinterpret_cast<uint2*>(p.qa + qrow * (NO >> 1) + (oc0 >> 1)) = qc;
-                p.qsf[qrow * (NO >> 4) + (oc0 >> 4)] = static_cast<uint8_t>(qsb);
+        if (quant) {
+            // lanes 2t, 2t + 1: the two halves of token t's block (the
+            // 16-byte piece this lane just stored)
+            uint32_t qc;
+            const uint32_t qsb = nvfp4_quant_half8(v, qs, qc);
+            if (tok < t_end && oc0 < NO && row >= 0) {
+                *reinterpret_cast<uint32_t*>(p.qa + row * (NO >> 1) + (oc0 >> 1) + 4 * hh) = qc;
+                if (hh == 0) p.qsf[row * (NO >> 4) + (oc0 >> 4)] = static_cast<uint8_t>(qsb);
             }
         }
         __syncwarp();

@@ -31,11 +31,27 @@ __device__ __forceinline__ uint32_t nvfp4_block_scale(float amax, float& d) {
     return sf;
 }
 
+// z / d rounded to nearest even, from y = RN(1 / d): q0 = RN(z y), the
+// residual z - q0 d (exact with one fused multiply-add), q1 = RN(q0 + r y).
+// Markstein's theorem (P. Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; also
+// Muller et al., "Handbook of Floating-Point Arithmetic", on division from a
+// correctly rounded reciprocal) makes q1 the correctly rounded quotient when
+// no step underflows or overflows.  Here d is an e4m3 value (>= 2^-9) and a
+// quotient small enough for the residual to underflow is far below 0.25, so
+// its e2m1 code is 0 either way; a quotient never overflows (d saturates at
+// 448).  Three instructions per element instead of a full division.
+__device__ __forceinline__ float div_rn_by_recip(float z, float d, float y) {
+    const float q0 = __fmul_rn(z, y);
+    const float r = __fmaf_rn(-q0, d, z);
+    return __fmaf_rn(r, y, q0);
+}
+
 // One byte of two e2m1 codes: z_even / d in the low nibble, z_odd / d in the
-// high one; both +0 when d == 0.
-__device__ __forceinline__ uint32_t nvfp4_code_pair(float z_even, float z_odd, float d) {
+// high one (y = RN(1 / d)); both +0 when d == 0.
+__device__ __forceinline__ uint32_t nvfp4_code_pair(float z_even, float z_odd, float d, float y) {
     if (!(d > 0.f)) return 0u;
-    const float lo = __fdiv_rn(z_even, d), hi = __fdiv_rn(z_odd, d);
+    const float lo = div_rn_by_recip(z_even, d, y), hi = div_rn_by_recip(z_odd, d, y);
     uint16_t r;
     asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tmov.b16 %0, {t, 0};\n\t}"
         : "=h"(r)
@@ -62,10 +78,37 @@ __device__ __forceinline__ uint32_t nvfp4_quant_block16(const uint4& v0, const u
     }
     float d;
     const uint32_t s = nvfp4_block_scale(amax, d);
+    const float y = d > 0.f ? __frcp_rn(d) : 0.f;
     uint32_t out[2] = {0u, 0u};
 #pragma unroll
-    for (int j = 0; j < 8; ++j) out[j >> 2] |= nvfp4_code_pair(z[2 * j], z[2 * j + 1], d) << (8 * (j & 3));
+    for (int j = 0; j < 8; ++j)
+        out[j >> 2] |= nvfp4_code_pair(z[2 * j], z[2 * j + 1], d, y) << (8 * (j & 3));
     codes = make_uint2(out[0], out[1]);
+    return s;
+}
+
+// Half a block for two cooperating lanes (lane pairs l, l ^ 1, all 32 lanes
+// active): this lane's 8 bf16 values (one uint4), the partner's 8 complete
+// the block.  Same steps and bits as nvfp4_quant_block16; returns the scale
+// byte and this lane's 4 code bytes (elements 8h .. 8h + 7 of the block).
+__device__ __forceinline__ uint32_t nvfp4_quant_half8(const uint4& v, float q, uint32_t& codes) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float z[8];
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        z[2 * j] = __fmul_rn(__uint_as_float(w[j] << 16), q);
+        z[2 * j + 1] = __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), q);
+        amax = fmaxf(amax, fmaxf(fabsf(z[2 * j]), fabsf(z[2 * j + 1])));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    float d;
+    const uint32_t s = nvfp4_block_scale(amax, d);
+    const float y = d > 0.f ? __frcp_rn(d) : 0.f;
+    uint32_t out = 0u;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) out |= nvfp4_code_pair(z[2 * j], z[2 * j + 1], d, y) << (8 * j);
+    codes = out;
     return s;
 }
 

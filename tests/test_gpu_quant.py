@@ -107,6 +107,27 @@ def test_quantize_matches_oracle(lib, R, L, rps, kind, qkind):
     np.testing.assert_array_equal(codes, want_c)
 
 
+def test_quantize_near_ties_for_every_scale(lib):
+    """Quotients z / d at, and one to three float32 ulps around, every
+    midpoint of the e2m1 grid, for every positive finite e4m3 scale d: each
+    block's largest element is 6, so with the pre-scale q = d (1 + k 2^-23)
+    the block scale is d and element m gives z / d ~ m (1 + k 2^-23).  Codes
+    and scales must match the oracle's correctly rounded float32 division
+    and e2m1 rounding bit for bit (the encoder divides through one rounded
+    reciprocal per block and a residual correction)."""
+    mids = np.float32([6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0,
+                       -0.25, -0.75, -1.25, -1.75, -2.5, -3.5, -5.0, 0.5])
+    xb = (mids.view(np.uint32) >> 16).astype(np.uint16)          # exact in bf16
+    ds = oracle.E4M3_TABLE[1:0x7F].astype(np.float64)             # 126 scales
+    ks = np.arange(-3, 4, dtype=np.float64)
+    q = (ds[:, None] * (1.0 + ks[None, :] * 2.0 ** -23)).astype(np.float32).ravel()
+    x = np.tile(xb, (q.size, 1))
+    codes, sf = gpu_quantize(lib, x, q, 1)
+    want_c, want_sf = oracle.quantize_nvfp4(x, q)
+    np.testing.assert_array_equal(sf, want_sf)
+    np.testing.assert_array_equal(codes, want_c)
+
+
 def _pow2_prescale(y_max):
     """Power of two that brings the block maxima near the top of the NVFP4
     range (448 * 6), from the oracle's output."""
