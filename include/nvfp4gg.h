@@ -369,9 +369,17 @@ int nvfp4_grouped_gemm_nt_masked_swiglu_quant(const void* A, const void* A_sf, c
  * and h_masked_m directly, and its epilogue stores the valid rows of C
  * straight into h_C (16-byte aligned) over the CPU-GPU link.  Pageable
  * buffers go through d_staging instead: one copy each for alpha and
- * masked_m, and one device->host copy of C per non-empty expert.  Returns
- * when the work is queued; synchronise `stream` before reading h_C, and do
- * not modify the inputs before then.
+ * masked_m, and one device->host copy of C per non-empty expert.  Calls with
+ * M_max > 64 and at least 2 MiB of activations copy them in 2 to 4 expert
+ * chunks of growing size (1 : 4 : 16 : 64) on a library-owned stream, each
+ * chunk's GEMM waiting (by an event) for its own copy only, so that later
+ * chunks cross the link while earlier ones compute; the copies wait for the
+ * work queued on `stream` before the call, and the results equal the
+ * unchunked call's bit for bit.  Returns
+ * when the work is queued; synchronise `stream` (which then covers the
+ * side stream's copies) before reading h_C, and do not modify the inputs
+ * before then.  While `stream` is being captured into a CUDA graph, no
+ * other thread may call this entry point with a chunked shape.
  */
 size_t nvfp4_host_staging_bytes(int G, int M_max, int N, int K);
 int nvfp4_grouped_gemm_nt_masked_host(const void* h_A, const void* h_A_sf,

@@ -111,7 +111,7 @@ struct TokenMaps {
     CUtensorMap a[kMaxWidths];
     CUtensorMap asf[kMaxWidths];
 };
-constexpr int kMapCache = 8;
+constexpr int kMapCache = 16;
 TokenMaps g_maps[kMapCache];
 int g_maps_next = 0;
 
@@ -286,7 +286,7 @@ struct WeightMap {
     int dev = -1;
     CUtensorMap m;
 };
-constexpr int kWeightMapCache = 4;
+constexpr int kWeightMapCache = 16;
 WeightMap g_wmaps[kWeightMapCache];
 int g_wmaps_next = 0;
 
@@ -810,6 +810,70 @@ void* host_mapped(const void* h) {
     return a.devicePointer;
 }
 
+// The host-buffer entry copies large activations in expert chunks on a side
+// stream, so that later chunks cross the CPU-GPU link while earlier chunks'
+// GEMMs run (measured on GB300: host-to-device copies and the GEMM's stores
+// into host memory share the link only in part).  The chunks grow fourfold
+// (experts in the ratio 1 : 4 : 16 : 64): the first copy, which nothing
+// hides, stays short, and each further copy still ends before the previous
+// chunk's GEMM, whose output is several times its input in every prefill
+// shape.  Per device: the side stream, an event marking the caller's stream
+// at entry, and one event per chunk that the chunk's GEMM waits for.
+// Created on first use; nvfp4_gg_shutdown forgets them (after a device
+// reset they are gone with the context).
+constexpr int kHostChunks = 4;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t copy = nullptr;
+    cudaEvent_t entry = nullptr;
+    cudaEvent_t chunk[kHostChunks] = {};
+};
+std::mutex g_host_mu;   // held over a call's whole enqueue; taken before g_mu, never after it
+HostPipe g_pipe[kMaxDevices];
+
+// The current device's pipe; the caller holds g_host_mu.
+int host_pipe(HostPipe** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4GG_ERR_CUDA;
+    HostPipe& hp = g_pipe[dev];
+    if (!hp.ready) {
+        if (cudaStreamCreateWithFlags(&hp.copy, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp.entry, cudaEventDisableTiming) != cudaSuccess)
+            return NVFP4GG_ERR_CUDA;
+        for (int j = 0; j < kHostChunks; ++j)
+            if (cudaEventCreateWithFlags(&hp.chunk[j], cudaEventDisableTiming) != cudaSuccess)
+                return NVFP4GG_ERR_CUDA;
+        hp.ready = true;
+    }
+    *out = &hp;
+    return NVFP4GG_OK;
+}
+
+// Expert chunks of the host-buffer entry: end[j] is one past chunk j's last
+// expert; returns the number of chunks.  One chunk unless the call has
+// prefill-sized experts (M_max > 64: the plain entry never splits K there,
+// so every chunk runs the kernel the whole call would) and at least 2 MiB of
+// activations; two from 2 MiB, three from 8 MiB, four from 32 MiB, never
+// more than G.  Chunk j holds about G 4^j / (1 + 4 + ... + 4^(P-1))
+// experts, at least one.
+int host_chunks(int G, int M_max, size_t in_bytes, int* end) {
+    int P = 1;
+    if (M_max > 64 && G <= TokPairCfg::MAX_GROUPS)
+        P = in_bytes >= (32u << 20) ? 4 : in_bytes >= (8u << 20) ? 3 : in_bytes >= (2u << 20) ? 2 : 1;
+    if (P > G) P = G;
+    const long long total = ((1LL << (2 * P)) - 1) / 3;   // 1 + 4 + ... + 4^(P-1)
+    long long cum = 0;
+    int prev = 0;
+    for (int j = 0; j < P; ++j) {
+        cum += 1LL << (2 * j);
+        int e = (int)((G * cum + total / 2) / total);
+        if (e < prev + 1) e = prev + 1;
+        if (e > G - (P - 1 - j)) e = G - (P - 1 - j);
+        end[j] = prev = e;
+    }
+    return P;
+}
+
 }  // namespace
 
 extern "C" {
@@ -852,9 +916,24 @@ int nvfp4_grouped_gemm_nt_masked_host(const void* h_A, const void* h_A_sf, const
     const int* mask_in = static_cast<const int*>(host_mapped(h_masked_m));
     void* c_out = host_mapped(h_C);
     if (c_out && !aligned(c_out, 16)) c_out = nullptr;
-    if (cudaMemcpyAsync(dA, h_A, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
-        cudaMemcpyAsync(dAsf, h_A_sf, asf_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    const size_t group_bytes = (size_t)M_max * N * 2;
+    int chunk_end[kHostChunks];
+    const int P = host_chunks(G, M_max, a_bytes + asf_bytes, chunk_end);
+    std::unique_lock<std::mutex> pipe_lock(g_host_mu, std::defer_lock);
+    HostPipe* hp = nullptr;
+    if (P > 1) {
+        pipe_lock.lock();
+        if ((rc = host_pipe(&hp)) != NVFP4GG_OK) return rc;
+        // the side stream's copies may overwrite the staging buffer only
+        // after the work queued on `stream` before this call (a previous
+        // call's GEMM still reading it)
+        if (cudaEventRecord(hp->entry, st) != cudaSuccess ||
+            cudaStreamWaitEvent(hp->copy, hp->entry, 0) != cudaSuccess)
+            return NVFP4GG_ERR_CUDA;
+    } else if (cudaMemcpyAsync(dA, h_A, a_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+               cudaMemcpyAsync(dAsf, h_A_sf, asf_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) {
         return NVFP4GG_ERR_CUDA;
+    }
     if (!alpha_in) {
         if (cudaMemcpyAsync(dAlpha, h_alpha, (size_t)G * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
             return NVFP4GG_ERR_CUDA;
@@ -865,10 +944,35 @@ int nvfp4_grouped_gemm_nt_masked_host(const void* h_A, const void* h_A_sf, const
             return NVFP4GG_ERR_CUDA;
         mask_in = dMask;
     }
-    rc = nvfp4_grouped_gemm_nt_masked(dA, dAsf, B, B_sf, alpha_in, mask_in, c_out ? c_out : dC, G,
-                                      M_max, N, K, stream);
+    uint8_t* c_dst = static_cast<uint8_t*>(c_out ? c_out : dC);
+    if (P == 1) {
+        rc = nvfp4_grouped_gemm_nt_masked(dA, dAsf, B, B_sf, alpha_in, mask_in, c_dst, G, M_max, N,
+                                          K, stream);
+    } else {
+        // chunk j: its experts' rows of A and A_sf copied on the side
+        // stream, its GEMM on `stream` after that copy
+        size_t b_expert = 0, sf_expert = 0;
+        if ((rc = nvfp4_prepared_weight_bytes(1, N, K, &b_expert, &sf_expert)) != NVFP4GG_OK)
+            return rc;
+        const size_t a_row = (size_t)K / 2, sf_row = (size_t)K / 16;
+        for (int j = 0; j < P && rc == NVFP4GG_OK; ++j) {
+            const int g0 = j == 0 ? 0 : chunk_end[j - 1];
+            const int g1 = chunk_end[j];
+            const size_t r0 = (size_t)g0 * M_max, nr = (size_t)(g1 - g0) * M_max;
+            if (cudaMemcpyAsync(dA + r0 * a_row, static_cast<const uint8_t*>(h_A) + r0 * a_row,
+                                nr * a_row, cudaMemcpyHostToDevice, hp->copy) != cudaSuccess ||
+                cudaMemcpyAsync(dAsf + r0 * sf_row, static_cast<const uint8_t*>(h_A_sf) + r0 * sf_row,
+                                nr * sf_row, cudaMemcpyHostToDevice, hp->copy) != cudaSuccess ||
+                cudaEventRecord(hp->chunk[j], hp->copy) != cudaSuccess ||
+                cudaStreamWaitEvent(st, hp->chunk[j], 0) != cudaSuccess)
+                return NVFP4GG_ERR_CUDA;
+            rc = nvfp4_grouped_gemm_nt_masked(
+                dA + r0 * a_row, dAsf + r0 * sf_row, static_cast<const uint8_t*>(B) + g0 * b_expert,
+                static_cast<const uint8_t*>(B_sf) + g0 * sf_expert, alpha_in + g0, mask_in + g0,
+                c_dst + g0 * group_bytes, g1 - g0, M_max, N, K, stream);
+        }
+    }
     if (rc != NVFP4GG_OK || c_out) return rc;
-    const size_t group_bytes = (size_t)M_max * N * 2;
     for (int g = 0; g < G; ++g) {
         if (h_masked_m[g] == 0) continue;
         if (cudaMemcpyAsync(static_cast<uint8_t*>(h_C) + g * group_bytes, dC + g * group_bytes,
@@ -1046,9 +1150,11 @@ extern "C" int nvfp4_grouped_gemm_nt_masked_splitk_noalloc(
 extern "C" {
 
 int nvfp4_gg_shutdown(void) {
+    std::lock_guard<std::mutex> pipe_lock(g_host_mu);
     std::lock_guard<std::mutex> lock(g_mu);
     for (int i = 0; i < kMaxDevices; ++i) {
         g_dev[i] = DeviceState{};
+        g_pipe[i] = HostPipe{};
         g_signal_addr[i] = nullptr;
         g_noalloc_addr[i] = nullptr;
     }

@@ -329,6 +329,48 @@ def test_host_buffer_entry_point_matches_device_path(lib, pinned_in, pinned_out)
     check_full(d, hC.numpy().view(np.uint16))
 
 
+@pytest.mark.parametrize("G,M_max,N,K,pinned_out", [
+    (40, 128, 256, 4096, True),      # CTA pairs, 3 chunks of 2, 8, 30 experts
+    (40, 128, 256, 4096, False),     # the same with pageable C (staged, copied per expert)
+    (120, 128, 256, 4096, True),     # 4 chunks of 1, 6, 23, 90 experts
+    (12, 384, 256, 2048, True),      # token-major pairs, 2 chunks of 2, 10 experts
+])
+def test_host_buffer_entry_point_chunked_copies(lib, G, M_max, N, K, pinned_out):
+    """Large host-buffer calls copy the activations in expert chunks on a
+    side stream, each chunk's GEMM waiting for its own copy: the bits equal
+    the device-buffer call's and rows >= masked_m stay untouched.  A second
+    call on other inputs is queued right behind the first, through the same
+    staging buffer: its copies must wait for the first call's GEMMs, or the
+    first call's output would mix the two problems."""
+    from nvfp4_block_scaled_masked_gb300.device import Problem
+    rng = np.random.default_rng(G * 1000 + M_max)
+    masked = [int(x) for x in rng.integers(1, M_max + 1, G)]
+    masked[0], masked[5], masked[-1] = 0, M_max, 0
+    cfg = W.custom(G, M_max, N, K, masked_m=masked)
+    calls = []
+    for seed in (G + M_max, G + M_max + 1):
+        d = W.generate(cfg, seed=seed)
+        prob = Problem(d)
+        prob.run()
+        h = {k: torch.from_numpy(np.ascontiguousarray(d[k])).pin_memory()
+             for k in ("A", "A_sf", "alpha")}
+        h["masked_m"] = torch.from_numpy(d["masked_m"].astype(np.int32)).pin_memory()
+        hC = torch.from_numpy(np.full((cfg.G, cfg.M_max, cfg.N), W.SENTINEL_BF16, dtype=np.int16))
+        calls.append((d, prob, prob.C_bits(), h, hC.pin_memory() if pinned_out else hC))
+    nbytes = lib.nvfp4_host_staging_bytes(cfg.G, cfg.M_max, cfg.N, cfg.K)
+    staging = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    for _, prob, _, h, hC in calls:
+        lib.nvfp4_grouped_gemm_nt_masked_host(h["A"], h["A_sf"], h["alpha"], h["masked_m"],
+                                              prob.B_prep, prob.B_sf_prep, hC, cfg.G, cfg.M_max,
+                                              cfg.N, cfg.K, staging, nbytes)
+    torch.cuda.synchronize()
+    assert lib.nvfp4_gg_check_error() == 0
+    for _, _, want, _, hC in calls:
+        np.testing.assert_array_equal(hC.numpy().view(np.uint16), want)
+    check_full(calls[0][0], calls[0][4].numpy().view(np.uint16))
+
+
 @pytest.mark.parametrize("G,M_max,N,K,masked", [
     (3, 200, 384, 512, [200, 5, 130]),      # single-CTA wide kernel (N % 256 != 0)
     (3, 200, 512, 768, [200, 5, 130]),      # CTA-pair kernel (automatic mode)
