@@ -34,8 +34,9 @@
 //   warps 7..14   epilogue, two warps per lane quarter (one per half of the
 //                 256 columns): tcgen05.ld of the whole quarter-half (lane =
 //                 token, column = weight row), x alpha, bf16 pairs held in
-//                 registers; the accumulator is released at once, so the
-//                 stores overlap the next tile's main loop.  Stores go
+//                 registers; the accumulator is released once the last
+//                 load has landed, so the stores overlap the next tile's
+//                 main loop.  Stores go
 //                 through a per-warp [32 rows][64 B] transpose in shared
 //                 memory: each instruction writes 8 rows x 64 contiguous
 //                 bytes; rows m >= masked_m are skipped.
@@ -374,11 +375,15 @@ gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams<1> p,
                                                                  p.timeout_ns));
             if (!ok) break;
             tc_fence_after();
-            const float al = __ldg(p.alpha + tc.g);
+            const uint32_t alb = __float_as_uint(__ldg(p.alpha + tc.g));
+            const uint64_t al2 = ((uint64_t)alb << 32) | alb;
             const uint32_t tbase = tmem + ((uint32_t)(quad * 32) << 16) + 128 * half;
             // the whole accumulator quarter-half into registers as bf16 pairs,
             // in 16-column loads, each issued before the previous one is
-            // converted (the conversion overlaps the next load's latency)
+            // converted (the conversion overlaps the next load's latency); the
+            // accumulator is released as soon as the last load has landed,
+            // before the last 16 columns are converted: the next tile's MMAs
+            // wait for that release, the stores below overlap them
             uint32_t o[64];
             uint32_t ra[16], rb[16];
             tmem_ld_32x32b_x16(tbase, ra);
@@ -387,23 +392,21 @@ gemm_nt_masked_tok_pair_kernel(const __grid_constant__ GemmParams<1> p,
                 tmem_wait_ld_regs(ra);
                 tmem_ld_32x32b_x16(tbase + 16 * (c + 1), rb);
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    o[8 * c + j] = pack_bf16x2(al * __uint_as_float(ra[2 * j]),
-                                               al * __uint_as_float(ra[2 * j + 1]));
+                for (int j = 0; j < 8; ++j) o[8 * c + j] = scale_pack_bf16x2(ra[2 * j], ra[2 * j + 1], al2);
                 tmem_wait_ld_regs(rb);
-                if (c + 2 < 8) tmem_ld_32x32b_x16(tbase + 16 * (c + 2), ra);
+                if (c + 2 < 8) {
+                    tmem_ld_32x32b_x16(tbase + 16 * (c + 2), ra);
+                } else {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (leader) mbar_arrive(acce_target);
+                        else mbar_arrive_remote_relaxed(acce_target);
+                    }
+                }
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    o[8 * (c + 1) + j] = pack_bf16x2(al * __uint_as_float(rb[2 * j]),
-                                                     al * __uint_as_float(rb[2 * j + 1]));
-            }
-            // TMEM is free: the next tile's MMAs may start while this warp
-            // stores (the stores overlap that tile's main loop)
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (leader) mbar_arrive(acce_target);
-                else mbar_arrive_remote_relaxed(acce_target);
+                    o[8 * (c + 1) + j] = scale_pack_bf16x2(rb[2 * j], rb[2 * j + 1], al2);
             }
             // stores: per 32-column chunk, a [32 rows][64 B] transpose in this
             // warp's staging buffer (16-byte units XOR-swizzled by row), then

@@ -508,4 +508,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// pack_bf16x2(alpha * lo, alpha * hi) for fp32 bit patterns lo, hi, with
+// both products from one packed fp32 multiply (each element rounded to
+// nearest even, as two scalar multiplies would be).  al2 holds alpha in both
+// halves.
+__device__ __forceinline__ uint32_t scale_pack_bf16x2(uint32_t lo, uint32_t hi, uint64_t al2) {
+    uint32_t r;
+    asm("{\n\t.reg .b64 v, p;\n\t.reg .b32 pl, ph;\n\t"
+        "mov.b64 v, {%1, %2};\n\t"
+        "mul.rn.f32x2 p, v, %3;\n\t"
+        "mov.b64 {pl, ph}, p;\n\t"
+        "cvt.rn.bf16x2.f32 %0, ph, pl;\n\t}"
+        : "=r"(r)
+        : "r"(lo), "r"(hi), "l"(al2));
+    return r;
+}
+
 }  // namespace nvfp4gg
