@@ -344,6 +344,7 @@ __device__ __forceinline__ void swiglu_tile_store(const GemmArgs& p, const int* 
     const int t_end = min(tc.t0 + tc.w, tc.m);
     const bool quant = p.qa != nullptr;
     const float qs = quant ? __ldg(p.qscale + tc.g) : 0.f;
+    const uint64_t al2 = ((uint64_t)__float_as_uint(al) << 32) | __float_as_uint(al);
     __nv_bfloat16* sb = reinterpret_cast<__nv_bfloat16*>(stage_buf);
 #pragma unroll 1
     for (int c = 0; c < TT_MAX / 16; ++c) {
@@ -357,8 +358,9 @@ __device__ __forceinline__ void swiglu_tile_store(const GemmArgs& p, const int* 
         const bool lo = lane < 16;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const float h0 = al * __uint_as_float(r[2 * j]);
-            const float h1 = al * __uint_as_float(r[2 * j + 1]);
+            uint32_t h0b, h1b;
+            mul2_rn(r[2 * j], r[2 * j + 1], al2, h0b, h1b);   // x alpha, two per instruction
+            const float h0 = __uint_as_float(h0b), h1 = __uint_as_float(h1b);
             const float p0 = __shfl_xor_sync(0xffffffffu, h0, 16);
             const float p1 = __shfl_xor_sync(0xffffffffu, h1, 16);
             const float gate = lo ? h0 : p1;

@@ -31,84 +31,126 @@ __device__ __forceinline__ uint32_t nvfp4_block_scale(float amax, float& d) {
     return sf;
 }
 
-// z / d rounded to nearest even, from y = RN(1 / d): q0 = RN(z y), the
-// residual z - q0 d (exact with one fused multiply-add), q1 = RN(q0 + r y).
-// Markstein's theorem (P. Markstein, "Computation of elementary functions on
-// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990; also
-// Muller et al., "Handbook of Floating-Point Arithmetic", on division from a
-// correctly rounded reciprocal) makes q1 the correctly rounded quotient when
-// no step underflows or overflows.  Here d is an e4m3 value (>= 2^-9) and a
-// quotient small enough for the residual to underflow is far below 0.25, so
-// its e2m1 code is 0 either way; a quotient never overflows (d saturates at
-// 448).  Three instructions per element instead of a full division.
-__device__ __forceinline__ float div_rn_by_recip(float z, float d, float y) {
-    const float q0 = __fmul_rn(z, y);
-    const float r = __fmaf_rn(-q0, d, z);
-    return __fmaf_rn(r, y, q0);
+// (a0 * b, a1 * b) for fp32 bit patterns a0, a1, from one packed fp32
+// multiply (each element rounded to nearest even, as a scalar multiply);
+// b2 holds b in both halves.
+__device__ __forceinline__ void mul2_rn(uint32_t a0, uint32_t a1, uint64_t b2, uint32_t& r0,
+                                        uint32_t& r1) {
+    asm("{\n\t.reg .b64 a, r;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mul.rn.f32x2 r, a, %4;\n\t"
+        "mov.b64 {%0, %1}, r;\n\t}"
+        : "=r"(r0), "=r"(r1)
+        : "r"(a0), "r"(a1), "l"(b2));
 }
 
-// One byte of two e2m1 codes: z_even / d in the low nibble, z_odd / d in the
-// high one (y = RN(1 / d)); both +0 when d == 0.
-__device__ __forceinline__ uint32_t nvfp4_code_pair(float z_even, float z_odd, float d, float y) {
-    if (!(d > 0.f)) return 0u;
-    const float lo = div_rn_by_recip(z_even, d, y), hi = div_rn_by_recip(z_odd, d, y);
-    uint16_t r;
-    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tmov.b16 %0, {t, 0};\n\t}"
-        : "=h"(r)
-        : "f"(lo), "f"(hi));
-    uint32_t b = r & 0xFFu;
-    if ((b & 0x07u) == 0) b &= 0xF0u;   // -0 -> +0
-    if ((b & 0x70u) == 0) b &= 0x0Fu;
-    return b;
-}
-
-// One 16-element block: bf16 values in v0 (elements 0..7) and v1 (8..15),
-// two per 32-bit word, low half first; pre-scale q.  Returns the scale byte
-// and leaves the 8 code bytes in codes.
-__device__ __forceinline__ uint32_t nvfp4_quant_block16(const uint4& v0, const uint4& v1, float q,
-                                                        uint2& codes) {
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    float z[16];
-    float amax = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        z[2 * j] = __fmul_rn(__uint_as_float(w[j] << 16), q);
-        z[2 * j + 1] = __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), q);
-        amax = fmaxf(amax, fmaxf(fabsf(z[2 * j]), fabsf(z[2 * j + 1])));
-    }
-    float d;
-    const uint32_t s = nvfp4_block_scale(amax, d);
-    const float y = d > 0.f ? __frcp_rn(d) : 0.f;
-    uint32_t out[2] = {0u, 0u};
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        out[j >> 2] |= nvfp4_code_pair(z[2 * j], z[2 * j + 1], d, y) << (8 * (j & 3));
-    codes = make_uint2(out[0], out[1]);
-    return s;
+// Four code bytes: byte j encodes (ze[j] / d, zo[j] / d), the even element
+// in the low nibble, with y2 = (y, y), y = RN(1 / d), and nd2 = (-d, -d).
+// Each quotient z / d, rounded to nearest even, comes from the rounded
+// reciprocal: q0 = RN(z y), the residual r = z - q0 d (exact with one fused
+// multiply-add), q1 = RN(q0 + r y).  Markstein's theorem (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990; also Muller et al., "Handbook of
+// Floating-Point Arithmetic", on division from a correctly rounded
+// reciprocal) makes q1 the correctly rounded quotient when no step
+// underflows or overflows.  Here d is an e4m3 value (>= 2^-9) and a quotient
+// small enough for the residual to underflow is far below 0.25, so its e2m1
+// code is 0 either way; a quotient never overflows (d saturates at 448).
+// The steps run two elements per packed fp32 instruction (each element
+// rounded as the scalar instruction would), then the saturating e2m1
+// conversions; -0 codes become +0 on all eight nibbles at once (a nibble
+// keeps its sign bit only if its magnitude bits are not all zero).
+__device__ __forceinline__ uint32_t nvfp4_code_quad(const uint32_t (&ze)[4],
+                                                    const uint32_t (&zo)[4], uint64_t y2,
+                                                    uint64_t nd2) {
+    uint32_t out;
+    asm("{\n\t.reg .b64 z, q0, r, q1;\n\t.reg .b32 l, h;\n\t.reg .b8 t0, t1, t2, t3;\n\t"
+        "mov.b64 z, {%1, %2};\n\t"
+        "mul.rn.f32x2 q0, z, %9;\n\t"
+        "fma.rn.f32x2 r, q0, %10, z;\n\t"
+        "fma.rn.f32x2 q1, r, %9, q0;\n\t"
+        "mov.b64 {l, h}, q1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t0, h, l;\n\t"
+        "mov.b64 z, {%3, %4};\n\t"
+        "mul.rn.f32x2 q0, z, %9;\n\t"
+        "fma.rn.f32x2 r, q0, %10, z;\n\t"
+        "fma.rn.f32x2 q1, r, %9, q0;\n\t"
+        "mov.b64 {l, h}, q1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t1, h, l;\n\t"
+        "mov.b64 z, {%5, %6};\n\t"
+        "mul.rn.f32x2 q0, z, %9;\n\t"
+        "fma.rn.f32x2 r, q0, %10, z;\n\t"
+        "fma.rn.f32x2 q1, r, %9, q0;\n\t"
+        "mov.b64 {l, h}, q1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t2, h, l;\n\t"
+        "mov.b64 z, {%7, %8};\n\t"
+        "mul.rn.f32x2 q0, z, %9;\n\t"
+        "fma.rn.f32x2 r, q0, %10, z;\n\t"
+        "fma.rn.f32x2 q1, r, %9, q0;\n\t"
+        "mov.b64 {l, h}, q1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 t3, h, l;\n\t"
+        "mov.b32 %0, {t0, t1, t2, t3};\n\t}"
+        : "=r"(out)
+        : "r"(ze[0]), "r"(zo[0]), "r"(ze[1]), "r"(zo[1]), "r"(ze[2]), "r"(zo[2]), "r"(ze[3]),
+          "r"(zo[3]), "l"(y2), "l"(nd2));
+    const uint32_t mag = out & 0x77777777u;
+    return mag | (out & ((mag + 0x77777777u) & 0x88888888u));
 }
 
 // Half a block for two cooperating lanes (lane pairs l, l ^ 1, all 32 lanes
 // active): this lane's 8 bf16 values (one uint4), the partner's 8 complete
-// the block.  Same steps and bits as nvfp4_quant_block16; returns the scale
+// the block.  Same steps and bits as nvfp4_quant_block16, the per-element
+// arithmetic two elements per packed fp32 instruction; returns the scale
 // byte and this lane's 4 code bytes (elements 8h .. 8h + 7 of the block).
 __device__ __forceinline__ uint32_t nvfp4_quant_half8(const uint4& v, float q, uint32_t& codes) {
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    float z[8];
+    const uint32_t qb = __float_as_uint(q);
+    const uint64_t q2 = ((uint64_t)qb << 32) | qb;
+    uint32_t ze[4], zo[4];
     float amax = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        z[2 * j] = __fmul_rn(__uint_as_float(w[j] << 16), q);
-        z[2 * j + 1] = __fmul_rn(__uint_as_float(w[j] & 0xFFFF0000u), q);
-        amax = fmaxf(amax, fmaxf(fabsf(z[2 * j]), fabsf(z[2 * j + 1])));
+        mul2_rn(w[j] << 16, w[j] & 0xFFFF0000u, q2, ze[j], zo[j]);
+        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(ze[j])), fabsf(__uint_as_float(zo[j]))));
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     float d;
     const uint32_t s = nvfp4_block_scale(amax, d);
-    const float y = d > 0.f ? __frcp_rn(d) : 0.f;
-    uint32_t out = 0u;
+    if (!(d > 0.f)) {
+        codes = 0u;
+        return s;
+    }
+    const uint32_t yb = __float_as_uint(__frcp_rn(d)), ndb = __float_as_uint(-d);
+    codes = nvfp4_code_quad(ze, zo, ((uint64_t)yb << 32) | yb, ((uint64_t)ndb << 32) | ndb);
+    return s;
+}
+
+// One 16-element block: bf16 values in v0 (elements 0..7) and v1 (8..15),
+// two per 32-bit word, low half first; pre-scale q.  Returns the scale byte
+// and leaves the 8 code bytes in codes.  The same steps and helpers as
+// nvfp4_quant_half8, one thread per block.
+__device__ __forceinline__ uint32_t nvfp4_quant_block16(const uint4& v0, const uint4& v1, float q,
+                                                        uint2& codes) {
+    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    const uint32_t qb = __float_as_uint(q);
+    const uint64_t q2 = ((uint64_t)qb << 32) | qb;
+    uint32_t ze[2][4], zo[2][4];
+    float amax = 0.f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) out |= nvfp4_code_pair(z[2 * j], z[2 * j + 1], d, y) << (8 * j);
-    codes = out;
+    for (int j = 0; j < 8; ++j) {
+        mul2_rn(w[j] << 16, w[j] & 0xFFFF0000u, q2, ze[j >> 2][j & 3], zo[j >> 2][j & 3]);
+        amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(ze[j >> 2][j & 3])),
+                                 fabsf(__uint_as_float(zo[j >> 2][j & 3]))));
+    }
+    float d;
+    const uint32_t s = nvfp4_block_scale(amax, d);
+    if (!(d > 0.f)) {
+        codes = make_uint2(0u, 0u);
+        return s;
+    }
+    const uint32_t yb = __float_as_uint(__frcp_rn(d)), ndb = __float_as_uint(-d);
+    const uint64_t y2 = ((uint64_t)yb << 32) | yb, nd2 = ((uint64_t)ndb << 32) | ndb;
+    codes = make_uint2(nvfp4_code_quad(ze[0], zo[0], y2, nd2), nvfp4_code_quad(ze[1], zo[1], y2, nd2));
     return s;
 }
 
