@@ -334,6 +334,38 @@ __device__ __forceinline__ TileCoord decode_tile(const int* cum, const int* gm, 
 // 128-row weight block; the [16 tokens][16 columns] bf16 chunk is staged in
 // `stage_buf` (512 bytes) and stored, and with qa set lane t < 16 also
 // encodes token t's 16 columns as one NVFP4 block of GEMM2's K.
+// silu(g) u = g u / (1 + exp(-g)) for two (g, u) pairs, two elements per
+// packed fp32 instruction where the arithmetic allows: exp(-g) as
+// 2^(-g log2 e) from the approximate base-2 exponential, the quotient
+// through the approximate reciprocal (the SwiGLU output is held to the
+// GEMM's tolerance, not to a correctly rounded result), both flushing
+// subnormal results to zero (an exponential below 2^-126 leaves 1 + e at 1;
+// a reciprocal below 2^-126 leaves y far under the tolerance).  For
+// g -> -inf the denominator overflows and the reciprocal gives 0.
+__device__ __forceinline__ void silu_mul2(float ga, float gb, float ua, float ub, float& ya,
+                                          float& yb) {
+    const uint64_t neg_log2e2 = 0xBFB8AA3BBFB8AA3Bull;   // (-log2 e, -log2 e)
+    const uint64_t one2 = 0x3F8000003F800000ull;         // (1, 1)
+    asm("{\n\t.reg .b64 g, u, t, e, d, n, y;\n\t.reg .b32 ta, tb, ea, eb, ra, rb;\n\t"
+        "mov.b64 g, {%2, %3};\n\t"
+        "mov.b64 u, {%4, %5};\n\t"
+        "mul.rn.f32x2 t, g, %6;\n\t"
+        "mov.b64 {ta, tb}, t;\n\t"
+        "ex2.approx.ftz.f32 ea, ta;\n\t"
+        "ex2.approx.ftz.f32 eb, tb;\n\t"
+        "mov.b64 e, {ea, eb};\n\t"
+        "add.rn.f32x2 d, e, %7;\n\t"
+        "mov.b64 {ta, tb}, d;\n\t"
+        "rcp.approx.ftz.f32 ra, ta;\n\t"
+        "rcp.approx.ftz.f32 rb, tb;\n\t"
+        "mul.rn.f32x2 n, g, u;\n\t"
+        "mov.b64 d, {ra, rb};\n\t"
+        "mul.rn.f32x2 y, n, d;\n\t"
+        "mov.b64 {%0, %1}, y;\n\t}"
+        : "=f"(ya), "=f"(yb)
+        : "f"(ga), "f"(gb), "f"(ua), "f"(ub), "l"(neg_log2e2), "l"(one2));
+}
+
 template <int TT_MAX>
 __device__ __forceinline__ void swiglu_tile_store(const GemmArgs& p, const int* off,
                                                   const TileCoord& tc, uint32_t tbase, int block,
@@ -357,16 +389,22 @@ __device__ __forceinline__ void swiglu_tile_store(const GemmArgs& p, const int* 
         // column (lane l's gate, its own up)
         const bool lo = lane < 16;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            uint32_t h0b, h1b;
-            mul2_rn(r[2 * j], r[2 * j + 1], al2, h0b, h1b);   // x alpha, two per instruction
-            const float h0 = __uint_as_float(h0b), h1 = __uint_as_float(h1b);
-            const float p0 = __shfl_xor_sync(0xffffffffu, h0, 16);
-            const float p1 = __shfl_xor_sync(0xffffffffu, h1, 16);
-            const float gate = lo ? h0 : p1;
-            const float up = lo ? p0 : h1;
-            const float y = __fdividef(gate * up, 1.0f + __expf(-gate));   // silu(gate) * up
-            sb[(2 * j + (lo ? 0 : 1)) * 16 + (lane & 15)] = __float2bfloat16_rn(y);
+        for (int j = 0; j < 8; j += 2) {
+            float gate[2], up[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                uint32_t h0b, h1b;
+                mul2_rn(r[2 * (j + k)], r[2 * (j + k) + 1], al2, h0b, h1b);   // x alpha
+                const float h0 = __uint_as_float(h0b), h1 = __uint_as_float(h1b);
+                const float p0 = __shfl_xor_sync(0xffffffffu, h0, 16);
+                const float p1 = __shfl_xor_sync(0xffffffffu, h1, 16);
+                gate[k] = lo ? h0 : p1;
+                up[k] = lo ? p0 : h1;
+            }
+            float y0, y1;
+            silu_mul2(gate[0], gate[1], up[0], up[1], y0, y1);
+            sb[(2 * j + (lo ? 0 : 1)) * 16 + (lane & 15)] = __float2bfloat16_rn(y0);
+            sb[(2 * j + 2 + (lo ? 0 : 1)) * 16 + (lane & 15)] = __float2bfloat16_rn(y1);
         }
         __syncwarp();
         const int t = lane >> 1, hh = lane & 1;

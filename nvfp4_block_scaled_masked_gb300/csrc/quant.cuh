@@ -24,8 +24,15 @@
 namespace nvfp4gg {
 
 // e4m3 byte of the block scale for block maximum |z| = amax, and its value d.
+// amax / 6 rounded to nearest even from RN(1 / 6) and one residual
+// correction (the steps and the theorem of nvfp4_code_quad below); when the
+// residual underflows, amax / 6 is below 2^-126 and its e4m3 byte is 0
+// either way, and an infinite amax is passed through (inf / 6 = inf).
 __device__ __forceinline__ uint32_t nvfp4_block_scale(float amax, float& d) {
-    const float s = __fdiv_rn(amax, 6.0f);
+    const float y6 = __uint_as_float(0x3E2AAAABu);   // RN(1 / 6)
+    const float q0 = __fmul_rn(amax, y6);
+    const float q1 = __fmaf_rn(__fmaf_rn(-q0, 6.0f, amax), y6, q0);
+    const float s = amax == __uint_as_float(0x7F800000u) ? amax : q1;
     const uint32_t sf = __nv_cvt_float_to_fp8(s, __NV_SATFINITE, __NV_E4M3);
     d = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(sf), __NV_E4M3)));
     return sf;

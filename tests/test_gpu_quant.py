@@ -128,6 +128,26 @@ def test_quantize_near_ties_for_every_scale(lib):
     np.testing.assert_array_equal(codes, want_c)
 
 
+def test_block_scale_near_e4m3_midpoints(lib):
+    """Blocks whose amax / 6 lies at, and one to three float32 ulps around,
+    every midpoint between consecutive positive e4m3 values (and above the
+    largest, where the scale saturates): scale bytes and codes bit for bit
+    against the oracle's correctly rounded float32 quotient (the encoder
+    divides by 6 through RN(1/6) and one residual correction).  Each block's
+    largest magnitude is 6, so with the pre-scale q, amax / 6 ~ q."""
+    vals = oracle.E4M3_TABLE[1:0x7F].astype(np.float64)          # 126 positive finite
+    mids = np.concatenate([(vals[:-1] + vals[1:]) / 2.0, [464.0, 672.0]])
+    ks = np.arange(-3, 4, dtype=np.float64)
+    q = (mids[:, None] * (1.0 + ks[None, :] * 2.0 ** -23)).astype(np.float32).ravel()
+    row = np.float32([6.0, -3.0, 1.5, -0.75, 0.5, 2.0, -6.0, 0.25,
+                      4.0, -1.0, 3.0, 0.0, 5.0, -2.5, 1.0, -0.5])
+    x = np.tile((row.view(np.uint32) >> 16).astype(np.uint16), (q.size, 1))
+    codes, sf = gpu_quantize(lib, x, q, 1)
+    want_c, want_sf = oracle.quantize_nvfp4(x, q)
+    np.testing.assert_array_equal(sf, want_sf)
+    np.testing.assert_array_equal(codes, want_c)
+
+
 def _pow2_prescale(y_max):
     """Power of two that brings the block maxima near the top of the NVFP4
     range (448 * 6), from the oracle's output."""
