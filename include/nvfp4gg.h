@@ -419,11 +419,13 @@ int nvfp4_gg_set_pair_mode(int mode);
 /*
  * Drops every host-side cache of the library: per-device state (SM count,
  * error-word and scratch addresses, kernel attributes, cluster fits) and
- * the tensor-map caches.  The library holds no device allocation, so
- * nothing is freed on the device; the next call on a device sets it up
- * again.  Call it after a cudaDeviceReset, or when done with the library.
- * It must not run while another thread is inside a library call.  Returns
- * NVFP4GG_OK.
+ * the tensor-map caches, and forgets the host-buffer entry's side stream
+ * and events without destroying them (after a cudaDeviceReset they are
+ * gone with the context; otherwise the context releases them when it is
+ * destroyed).  The library holds no device allocation, so nothing is freed
+ * on the device; the next call on a device sets it up again.  Call it after
+ * a cudaDeviceReset, or when done with the library.  It must not run while
+ * another thread is inside a library call.  Returns NVFP4GG_OK.
  */
 int nvfp4_gg_shutdown(void);
 
