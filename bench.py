@@ -548,9 +548,10 @@ def main():
                    "how": ("(plain GEMM: the host-buffer entry point has no SwiGLU variant) "
                            if args.swiglu else "") +
                           "nvfp4_grouped_gemm_nt_masked_host on pinned host buffers: A and A_sf "
-                          "copied to the device, alpha and masked_m read and the valid rows of C "
-                          "written by the kernel in host memory, stream sync; wall clock per "
-                          "step (Python call included)"}
+                          "copied to the device (prefill-sized calls in up to four expert chunks "
+                          "on a side stream, each chunk's GEMM after its own copy), alpha and "
+                          "masked_m read and the valid rows of C written by the kernel in host "
+                          "memory, stream sync; wall clock per step (Python call included)"}
     line["clocks"] = sampler.summary()
 
     if rank == 0 and not args.no_cpu_baseline:
