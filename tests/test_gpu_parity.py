@@ -329,13 +329,14 @@ def test_host_buffer_entry_point_matches_device_path(lib, pinned_in, pinned_out)
     check_full(d, hC.numpy().view(np.uint16))
 
 
-@pytest.mark.parametrize("G,M_max,N,K,pinned_out", [
-    (40, 128, 256, 4096, True),      # CTA pairs, 3 chunks of 2, 8, 30 experts
-    (40, 128, 256, 4096, False),     # the same with pageable C (staged, copied per expert)
-    (120, 128, 256, 4096, True),     # 4 chunks of 1, 6, 23, 90 experts
-    (12, 384, 256, 2048, True),      # token-major pairs, 2 chunks of 2, 10 experts
+@pytest.mark.parametrize("G,M_max,N,K,pinned_in,pinned_out", [
+    (40, 128, 256, 4096, True, True),     # CTA pairs, 3 chunks of 2, 8, 30 experts
+    (40, 128, 256, 4096, True, False),    # the same with pageable C (staged, copied per expert)
+    (40, 128, 256, 4096, False, True),    # pageable activations, alpha and masked_m
+    (120, 128, 256, 4096, True, True),    # 4 chunks of 1, 6, 23, 90 experts
+    (12, 384, 256, 2048, True, True),     # token-major pairs, 2 chunks of 2, 10 experts
 ])
-def test_host_buffer_entry_point_chunked_copies(lib, G, M_max, N, K, pinned_out):
+def test_host_buffer_entry_point_chunked_copies(lib, G, M_max, N, K, pinned_in, pinned_out):
     """Large host-buffer calls copy the activations in expert chunks on a
     side stream, each chunk's GEMM waiting for its own copy: the bits equal
     the device-buffer call's and rows >= masked_m stay untouched.  A second
@@ -352,9 +353,10 @@ def test_host_buffer_entry_point_chunked_copies(lib, G, M_max, N, K, pinned_out)
         d = W.generate(cfg, seed=seed)
         prob = Problem(d)
         prob.run()
-        h = {k: torch.from_numpy(np.ascontiguousarray(d[k])).pin_memory()
-             for k in ("A", "A_sf", "alpha")}
-        h["masked_m"] = torch.from_numpy(d["masked_m"].astype(np.int32)).pin_memory()
+        h = {k: torch.from_numpy(np.ascontiguousarray(d[k])) for k in ("A", "A_sf", "alpha")}
+        h["masked_m"] = torch.from_numpy(d["masked_m"].astype(np.int32))
+        if pinned_in:
+            h = {k: v.pin_memory() for k, v in h.items()}
         hC = torch.from_numpy(np.full((cfg.G, cfg.M_max, cfg.N), W.SENTINEL_BF16, dtype=np.int16))
         calls.append((d, prob, prob.C_bits(), h, hC.pin_memory() if pinned_out else hC))
     nbytes = lib.nvfp4_host_staging_bytes(cfg.G, cfg.M_max, cfg.N, cfg.K)
