@@ -7,8 +7,9 @@ synthetic workload (default: the largest single-GPU workload, the prefill
 GEMM2 of a 256-expert MoE layer: G=256, masked_m from top-8 routing of 4096
 tokens, M_max=256, N=7168, K=2048, 962 GFLOP and 2.6 GB per call).  The same
 run also times the other four workloads (decode GEMM1 at 32 and 256 experts,
-the compute-bound G=8 M=2048 shape and the small masked case) and reports
-them under "per_config", with sampled parity against the oracle.  Each timed step is bracketed by
+the compute-bound G=8 M=2048 shape and the small masked case) and the fused
+MoE GEMM1 epilogue (SwiGLU + NVFP4 output, the same shape taken as GEMM1)
+and reports them under "per_config", with sampled parity against the oracle.  Each timed step is bracketed by
 CUDA events on the launching stream; between steps L2 is flushed by writing a
 256 MB buffer and then reading it back, so the next step starts with an L2
 that holds none of its inputs and no dirty lines.  Prints one JSON line (rank 0).  Under torchrun every rank runs an
@@ -322,6 +323,62 @@ def per_config_block(args, peaks, probe_best, main_key, main_ms, main_d, main_C,
     return out, kept
 
 
+SWIGLU_QUANT_KEY = "c4_swiglu_quant"
+SWIGLU_QUANT_QSCALE = 2.0 ** -9
+
+
+def swiglu_quant_entry(args, peaks, probe_best, d, flush, stream):
+    """GEMM1 + SwiGLU + NVFP4 output (nvfp4_grouped_gemm_nt_masked_swiglu_quant)
+    on the prefill workload's shape taken as GEMM1 (N = 2I gate and up rows):
+    device time and HBM fraction over its algorithmic bytes (weights and
+    activations once, the bf16 SwiGLU output, the e2m1 codes and e4m3
+    scales).  The outputs are kept for the sampled parity check."""
+    import torch
+    from nvfp4_block_scaled_masked_gb300 import binding
+    from nvfp4_block_scaled_masked_gb300.device import Problem
+    cfg = d["cfg"]
+    prob = Problem(d, keep_raw_weights=True)
+    binding.nvfp4_prepare_weights_swiglu(prob.raw_B, prob.raw_Bsf, cfg.G, cfg.N, cfg.K,
+                                         prob.B_prep, prob.B_sf_prep)
+    prob.raw_B = prob.raw_Bsf = prob.C = None
+    I = cfg.N // 2
+    C_half = torch.full((cfg.G, cfg.M_max, I), W.SENTINEL_BF16, dtype=torch.int16, device="cuda")
+    A2 = torch.zeros((cfg.G, cfg.M_max, I // 2), dtype=torch.uint8, device="cuda")
+    A2_sf = torch.zeros((cfg.G, cfg.M_max, I // 16), dtype=torch.uint8, device="cuda")
+    qscale = torch.full((cfg.G,), SWIGLU_QUANT_QSCALE, dtype=torch.float32, device="cuda")
+
+    def step():
+        binding.nvfp4_grouped_gemm_nt_masked_swiglu_quant(
+            prob.A, prob.A_sf, prob.B_prep, prob.B_sf_prep, prob.alpha, prob.masked_m, C_half,
+            qscale, A2, A2_sf, cfg.G, cfg.M_max, cfg.N, cfg.K)
+
+    for _ in range(3):
+        step()
+    if binding.nvfp4_gg_check_error() != 0:
+        raise RuntimeError("device error on the SwiGLU + NVFP4 entry")
+    ms_list = time_steps(step, args.per_config_steps, flush, stream)
+    if binding.nvfp4_gg_check_error() != 0:
+        raise RuntimeError("device error on the SwiGLU + NVFP4 entry")
+    ms = statistics.median(ms_list)
+    counts = W.algorithmic_counts(cfg, d["masked_m"])
+    counts["bytes"] -= counts["out_bytes"] // 2            # N/2 bf16 columns per valid row
+    counts["bytes"] += counts["rows"] * (cfg.N // 4 + cfg.N // 32)   # codes and scales
+    r = roofline_fracs(cfg, counts, ms, peaks, probe_best)
+    entry = {"workload": f"GEMM1 + SwiGLU + NVFP4 output on the shape of {cfg.name} "
+                         f"(N = {cfg.N} gate and up rows, {I} outputs per row)",
+             "entry_point": "nvfp4_grouped_gemm_nt_masked_swiglu_quant",
+             "ms": ms, "TFLOP/s": r["tflops"], "algorithmic_GB/s": r["gbs"], "bound": "hbm",
+             "frac_of_hbm": r["frac_hbm"], "frac_of_nvfp4_probe": r["frac_tensor"],
+             "traffic": None, "algorithmic_bytes": counts["bytes"], "flops": counts["flops"],
+             "steps": len(ms_list),
+             "timing": "median of steps, CUDA events, L2 flushed before each"}
+    kept = (d, C_half.cpu().numpy().view(np.uint16), A2.cpu().numpy(), A2_sf.cpu().numpy(),
+            SWIGLU_QUANT_QSCALE)
+    del prob, C_half, A2, A2_sf, qscale
+    torch.cuda.empty_cache()
+    return entry, kept
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -535,13 +592,17 @@ def main():
     if args.splitk >= 0 or args.swiglu:
         # the recorded DRAM traffic is the plain GEMM kernel's, not this entry point's
         line["roofline"]["traffic"] = None
-    kept = {}
+    kept, kept_sq = {}, None
     if args.per_config_steps > 0 and ws == 1:
         plain = args.splitk < 0 and not args.swiglu
         main_key = cfg.key if (plain and cfg.key in PER_CONFIG_KEYS) else None
         line["per_config"], kept = per_config_block(
             args, peaks, probe_best, main_key, ms, d, prob.C_bits() if main_key else None,
             flush, stream)
+        if plain:
+            d_sq = d if cfg.key == "c4" else W.generate(W.CONFIGS["c4"])
+            line["per_config"][SWIGLU_QUANT_KEY], kept_sq = swiglu_quant_entry(
+                args, peaks, probe_best, d_sq, flush, stream)
     line["e2e"] = {"value": counts["flops"] / (e2e_med / 1e3) / 1e12, "unit": UNIT,
                    "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                    "ms_per_step": e2e_med, "steps": args.e2e_steps,
@@ -558,6 +619,8 @@ def main():
         line["cpu_baseline"] = cpu_baseline(cfg, d, prob)
         for key, (dk, Ck) in kept.items():
             line["per_config"][key]["parity"] = sampled_parity(dk, Ck)
+        if kept_sq is not None:
+            line["per_config"][SWIGLU_QUANT_KEY]["parity"] = sampled_parity_swiglu(*kept_sq)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -723,6 +786,44 @@ def sampled_parity(d, C_bits, outputs: int = 20000, seed: int = 3):
     return {"outputs": int(ok.size), "within_tolerance": int(ok.sum()),
             "masked_rows_untouched": untouched,
             "sample": f"{outputs} random valid (g, m, n), fp64 oracle; max|ref| over the sample"}
+
+
+def sampled_parity_swiglu(d, C_bits, A2, A2_sf, q, outputs: int = 20000, rows: int = 64,
+                          seed: int = 5):
+    """Part of the CPU-baseline leg, for the SwiGLU + NVFP4 entry: random valid
+    SwiGLU outputs against silu(gate) * up from the oracle's sampled fp64 GEMM
+    (gate column j, up column I + j), the GEMM tolerance; rows m >= masked_m
+    compared with the prefill; and random valid rows' NVFP4 codes and scales
+    against the oracle's encoder applied to the GPU's own bf16 row, bit for
+    bit."""
+    from oracle import oracle
+    cfg = d["cfg"]
+    mm = d["masked_m"]
+    I = cfg.N // 2
+    untouched = all(bool(np.all(C_bits[g, mm[g]:] == W.SENTINEL_BF16)) for g in range(cfg.G))
+    rng = np.random.default_rng(seed)
+    valid_g = np.flatnonzero(mm > 0)
+    g = rng.choice(valid_g, outputs)
+    m = (rng.random(outputs) * mm[g]).astype(np.int64)
+    j = rng.integers(0, I, outputs)
+    args = (d["A"], d["A_sf"], d["B"], d["B_sf"], d["alpha"])
+    gate = oracle.gemm_sampled(*args, np.stack([g, m, j], 1).astype(np.int64),
+                               cfg.G, cfg.M_max, cfg.N, cfg.K)
+    up = oracle.gemm_sampled(*args, np.stack([g, m, I + j], 1).astype(np.int64),
+                             cfg.G, cfg.M_max, cfg.N, cfg.K)
+    ref = oracle.silu(gate) * up
+    vals = (C_bits[g, m, j].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    ok = oracle.tolerance_ok(vals, ref, np.abs(ref).max())
+    gr = rng.choice(valid_g, rows)
+    mr = (rng.random(rows) * mm[gr]).astype(np.int64)
+    want_c, want_sf = oracle.quantize_nvfp4(C_bits[gr, mr], np.full(rows, q, np.float32))
+    same = np.all(A2[gr, mr] == want_c, axis=1) & np.all(A2_sf[gr, mr] == want_sf, axis=1)
+    return {"outputs": int(ok.size), "within_tolerance": int(ok.sum()),
+            "masked_rows_untouched": untouched,
+            "nvfp4_rows": int(rows), "nvfp4_rows_bit_identical": int(same.sum()),
+            "sample": f"{outputs} random valid (g, m, j) SwiGLU outputs against the fp64 "
+                      f"oracle (max|ref| over the sample); {rows} random valid rows' codes and "
+                      "scales against the oracle's encoder on the GPU's bf16 row"}
 
 
 def cpu_baseline(cfg, d, prob):
